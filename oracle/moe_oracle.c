@@ -1,0 +1,320 @@
+/*
+ * moe_oracle.c -- CPU fp64 oracle of the MoE layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call
+ * this file: only the tests, the package's smoke check and the benchmark's CPU
+ * baseline use it. It shares no code, header or table with the CUDA library.
+ *
+ * It is a plain, slow, obviously correct restatement of what the pages define,
+ * in double precision end to end. Inputs are read exactly as the GPU receives
+ * them (fp32 or bf16 values widened to fp64, which is exact). OpenMP only
+ * splits independent tokens / rows across host threads.
+ *
+ * Sources (page titles as printed on the pages):
+ *   [P2] "MoE显存与计算开销四阶段手算指南": s2.1 gate projection logits = x @ W_g,
+ *        s2.2 softmax then per-token top-k (topk_indices / topk_probs),
+ *        s2.3 grouping of tokens per expert (N_i, sum N_i = B*S*k),
+ *        s2.4 weighted sum of the k expert outputs back in token order,
+ *        s3 the toy forward (stacked per-expert inputs, per-expert Linear).
+ *   [P3] "MoE混合专家模型计算原理与推理部署实战解析": s2.1 gate, softmax, top-k;
+ *        s2.2 renormalisation g_i' = g_i / sum of selected g and the weighted
+ *        output; s2.4 gate kept in fp32; s3.1 SwiGLU expert
+ *        (gate, up, SiLU(gate)*up, down); s5.1 count -> prefix sum -> permute ->
+ *        per-expert GEMM -> unpermute + weighted merge.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - top-k is taken on the score s = logit (+ per-expert bias); softmax is
+ *     monotone, so this is the pages' top-k over probabilities, without the
+ *     false ties that rounded probabilities can create;
+ *   - equal scores: the lower expert id wins; the k slots are in descending
+ *     score order;
+ *   - the bias (when given) is added to the logits before the softmax;
+ *   - rows of one expert are kept in flat assignment order t*k + j (stable);
+ *   - the two-matrix FFN uses the tanh form of GELU; no biases anywhere;
+ *   - weights are stored [out, in].
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F64 = 0, OR_F32 = 1, OR_BF16 = 2 };
+enum { OR_SWIGLU = 0, OR_GELU_TANH = 1 };
+
+/* Read element i of an input array stored as fp64, fp32 or bf16 bits. */
+static double rd(const void *p, int dt, int64_t i)
+{
+    if (dt == OR_F64) return ((const double *)p)[i];
+    if (dt == OR_F32) return (double)((const float *)p)[i];
+    uint32_t u = ((uint32_t)((const uint16_t *)p)[i]) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------------------
+ * Route: [P2] s2.1-2.2, [P3] s2.1-2.2.
+ *   l[t,n] = sum_i x[t,i] * W_g[i,n] (+ b[n])
+ *   p[t,:] = softmax(l[t,:])
+ *   top-k by l (ties -> lower id), in descending order
+ *   w[t,j] = p[t,e_j] / sum_j' p[t,e_j']
+ *
+ * Also returns, per token, what a parity test needs to judge an fp32
+ * evaluation of the same logits:
+ *   errb[t,n]  a bound on |fl32(l[t,n]) - l[t,n]| for ANY summation order:
+ *              gamma_{d+2} * (sum_i |x_i W_g[i,n]| + |b_n|), gamma_m = m u/(1-m u),
+ *              u = 2^-24 (the classical bound for a sum of d rounded products
+ *              plus one rounded bias addition);
+ *   cert[t]    min over i < k, j > i (sorted order) of
+ *              (l_(i) - errb_(i)) - (l_(j) + errb_(j)).
+ *              cert > 0 proves that an fp32 evaluation selects the same experts
+ *              in the same order.
+ *   logits     optional [T,N] copy of l.
+ * Returns 0, or -1 on bad arguments.
+ * ------------------------------------------------------------------------- */
+int oracle_route(int64_t T, int d, int N, int k,
+                 const void *x, int x_dt,
+                 const void *wg, int wg_dt,
+                 const void *bias, int b_dt,
+                 int32_t *topk_idx, double *topk_w,
+                 double *logits, double *errb, double *cert)
+{
+    if (T < 0 || d < 1 || N < 1 || k < 1 || k > N) return -1;
+    const double u = ldexp(1.0, -24);
+    const double gam = (d + 2) * u / (1.0 - (d + 2) * u);
+    int bad = 0;
+
+#pragma omp parallel
+    {
+        double *l = (double *)malloc(sizeof(double) * N);
+        double *s = (double *)malloc(sizeof(double) * N);
+        double *p = (double *)malloc(sizeof(double) * N);
+        double *eb = (double *)malloc(sizeof(double) * N);
+        int *taken = (int *)malloc(sizeof(int) * N);
+        int *order = (int *)malloc(sizeof(int) * N);
+        if (!l || !s || !p || !eb || !taken || !order) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < T; ++t) {
+                /* gate projection */
+                for (int n = 0; n < N; ++n) {
+                    double acc = 0.0, aabs = 0.0;
+                    for (int i = 0; i < d; ++i) {
+                        double prod = rd(x, x_dt, t * d + i) * rd(wg, wg_dt, (int64_t)i * N + n);
+                        acc += prod;
+                        aabs += fabs(prod);
+                    }
+                    double b = bias ? rd(bias, b_dt, n) : 0.0;
+                    l[n] = acc + b;
+                    s[n] = aabs + fabs(b);
+                    eb[n] = gam * s[n];
+                }
+                /* softmax over all N experts, with max subtraction */
+                double m = l[0];
+                for (int n = 1; n < N; ++n) if (l[n] > m) m = l[n];
+                double z = 0.0;
+                for (int n = 0; n < N; ++n) { p[n] = exp(l[n] - m); z += p[n]; }
+                for (int n = 0; n < N; ++n) p[n] /= z;
+                /* full descending order by (l desc, id asc): repeated argmax */
+                for (int n = 0; n < N; ++n) taken[n] = 0;
+                for (int r = 0; r < N; ++r) {
+                    int best = -1;
+                    for (int n = 0; n < N; ++n) {
+                        if (taken[n]) continue;
+                        if (best < 0 || l[n] > l[best]) best = n;   /* strict: lower id kept on ties */
+                    }
+                    taken[best] = 1;
+                    order[r] = best;
+                }
+                /* renormalise the k selected gate values */
+                double sel = 0.0;
+                for (int j = 0; j < k; ++j) sel += p[order[j]];
+                for (int j = 0; j < k; ++j) {
+                    topk_idx[t * k + j] = order[j];
+                    topk_w[t * k + j] = p[order[j]] / sel;
+                }
+                if (logits) for (int n = 0; n < N; ++n) logits[t * N + n] = l[n];
+                if (errb) for (int n = 0; n < N; ++n) errb[t * N + n] = eb[n];
+                if (cert) {
+                    double c = INFINITY;
+                    for (int i = 0; i < k; ++i) {
+                        double lo = l[order[i]] - eb[order[i]];
+                        for (int j2 = i + 1; j2 < N; ++j2) {
+                            double hi = l[order[j2]] + eb[order[j2]];
+                            if (lo - hi < c) c = lo - hi;
+                        }
+                    }
+                    cert[t] = c;
+                }
+            }
+        }
+        free(l); free(s); free(p); free(eb); free(taken); free(order);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Group assignments by expert: [P2] s2.3, [P3] s5.1 steps 2-3.
+ *   counts[n]  = number of (t,j) with e_{t,j} = n      (sum = T*k)
+ *   offsets    = exclusive prefix sum of counts, offsets[N] = T*k
+ *   rows of expert n are offsets[n] .. offsets[n+1]-1, filled in flat order
+ *   f = t*k + j:   perm[row] = t,  inv_perm[f] = row.
+ * Returns 0, or -1 if an index is out of [0, N).
+ * ------------------------------------------------------------------------- */
+int oracle_permute(int64_t T, int N, int k, const int32_t *topk_idx,
+                   int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm)
+{
+    const int64_t A = T * k;
+    for (int n = 0; n < N; ++n) counts[n] = 0;
+    for (int64_t f = 0; f < A; ++f) {
+        int e = topk_idx[f];
+        if (e < 0 || e >= N) return -1;
+        counts[e] += 1;
+    }
+    offsets[0] = 0;
+    for (int n = 0; n < N; ++n) offsets[n + 1] = offsets[n] + counts[n];
+    int32_t *fill = (int32_t *)malloc(sizeof(int32_t) * (size_t)N);
+    if (!fill) return -1;
+    for (int n = 0; n < N; ++n) fill[n] = offsets[n];
+    for (int64_t f = 0; f < A; ++f) {
+        int e = topk_idx[f];
+        int32_t row = fill[e]++;
+        perm[row] = (int32_t)(f / k);
+        inv_perm[f] = row;
+    }
+    free(fill);
+    return 0;
+}
+
+/* SiLU and tanh-GELU, [P3] s3.1 (SiLU(gate) * up). */
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+static double gelu_tanh(double v)
+{
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * v * (1.0 + tanh(c * (v + 0.044715 * v * v * v)));
+}
+
+/* ---------------------------------------------------------------------------
+ * One expert's FFN applied to n_rows input rows: [P3] s3.1, [P2] s2.3.
+ *   SwiGLU:   h = SiLU(W_gate x) * (W_up x),  y = W_down h
+ *   GELU:     h = gelu_tanh(W_1 x),           y = W_2 h     (w_up == NULL)
+ * W_gate, W_up: [F, d]; W_down: [d, F] (all [out, in]).
+ * x rows: [n_rows, d] in x_dt; y: [n_rows, d] fp64; h (optional): [n_rows, F].
+ * ------------------------------------------------------------------------- */
+int oracle_expert_rows(int64_t n_rows, int d, int F, int act,
+                       const void *x, int x_dt,
+                       const void *w_gate, const void *w_up, const void *w_down, int w_dt,
+                       double *y, double *h_out)
+{
+    if (d < 1 || F < 1 || (act != OR_SWIGLU && act != OR_GELU_TANH)) return -1;
+    if (act == OR_SWIGLU && !w_up) return -1;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xr = (double *)malloc(sizeof(double) * d);
+        double *h = (double *)malloc(sizeof(double) * F);
+        if (!xr || !h) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < n_rows; ++r) {
+                for (int i = 0; i < d; ++i) xr[i] = rd(x, x_dt, r * d + i);
+                for (int f = 0; f < F; ++f) {
+                    double g = 0.0;
+                    for (int i = 0; i < d; ++i) g += rd(w_gate, w_dt, (int64_t)f * d + i) * xr[i];
+                    if (act == OR_SWIGLU) {
+                        double up = 0.0;
+                        for (int i = 0; i < d; ++i) up += rd(w_up, w_dt, (int64_t)f * d + i) * xr[i];
+                        h[f] = silu(g) * up;
+                    } else {
+                        h[f] = gelu_tanh(g);
+                    }
+                }
+                if (h_out) for (int f = 0; f < F; ++f) h_out[r * F + f] = h[f];
+                for (int o = 0; o < d; ++o) {
+                    double acc = 0.0;
+                    for (int f = 0; f < F; ++f) acc += rd(w_down, w_dt, (int64_t)o * F + f) * h[f];
+                    y[r * d + o] = acc;
+                }
+            }
+        }
+        free(xr); free(h);
+    }
+    return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Combine: [P2] s2.4, [P3] s2.2 / s5.1 step 5.
+ *   out[t] = sum_{j<k} w[t,j] * y_perm[inv_perm[t*k+j]]   (j in order)
+ * Only the listed tokens (or all T when tokens == NULL) are written; out rows
+ * are [n_tok, d] in the order of the list.
+ * ------------------------------------------------------------------------- */
+int oracle_combine(int64_t n_tok, const int64_t *tokens, int d, int k,
+                   const double *y_perm, const int32_t *inv_perm, const double *topk_w,
+                   double *out)
+{
+    for (int64_t q = 0; q < n_tok; ++q) {
+        int64_t t = tokens ? tokens[q] : q;
+        for (int o = 0; o < d; ++o) out[q * d + o] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            double w = topk_w[t * k + j];
+            const double *yr = y_perm + (int64_t)inv_perm[t * k + j] * d;
+            for (int o = 0; o < d; ++o) out[q * d + o] += w * yr[o];
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Whole layer on small inputs, [P3] s6.1 steps 1-5 / s5.1:
+ *   route -> permute -> expert FFN per row -> combine.
+ * Expert weights are stacked [N,F,d] / [N,d,F]. y_perm [T*k, d] fp64 out,
+ * out [T, d] fp64. Routing outputs as in oracle_route / oracle_permute.
+ * ------------------------------------------------------------------------- */
+int oracle_forward(int64_t T, int d, int N, int k, int F, int act,
+                   const void *x, int x_dt, const void *wg, int wg_dt, const void *bias, int b_dt,
+                   const void *w_gate, const void *w_up, const void *w_down, int w_dt,
+                   int32_t *topk_idx, double *topk_w, double *cert,
+                   int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                   double *y_perm, double *out)
+{
+    const int64_t A = T * k;
+    int rc = oracle_route(T, d, N, k, x, x_dt, wg, wg_dt, bias, b_dt, topk_idx, topk_w, NULL, NULL, cert);
+    if (rc) return rc;
+    rc = oracle_permute(T, N, k, topk_idx, counts, offsets, perm, inv_perm);
+    if (rc) return rc;
+    /* gather the permuted input rows, then run each expert on its rows */
+    size_t es = (x_dt == OR_F64) ? 8 : (x_dt == OR_F32) ? 4 : 2;
+    unsigned char *xp = (unsigned char *)malloc(es * (size_t)(A > 0 ? A : 1) * (size_t)d);
+    if (!xp) return -1;
+    for (int64_t row = 0; row < A; ++row)
+        memcpy(xp + (size_t)row * d * es, (const unsigned char *)x + (size_t)perm[row] * d * es, (size_t)d * es);
+    size_t wes = (w_dt == OR_F64) ? 8 : (w_dt == OR_F32) ? 4 : 2;
+    for (int n = 0; n < N && rc == 0; ++n) {
+        int64_t r0 = offsets[n], nr = counts[n];
+        if (nr == 0) continue;
+        rc = oracle_expert_rows(nr, d, F, act, xp + (size_t)r0 * d * es, x_dt,
+                                (const unsigned char *)w_gate + (size_t)n * F * d * wes,
+                                w_up ? (const unsigned char *)w_up + (size_t)n * F * d * wes : NULL,
+                                (const unsigned char *)w_down + (size_t)n * d * F * wes, w_dt,
+                                y_perm + r0 * d, NULL);
+    }
+    free(xp);
+    if (rc) return rc;
+    return oracle_combine(T, NULL, d, k, y_perm, inv_perm, topk_w, out);
+}

@@ -1,0 +1,340 @@
+"""Pins of the CPU fp64 oracle against things the pages and mathematics fix.
+
+None of these re-types the oracle's loops: each check is an invariant the pages
+state, a closed form, a brute-force enumeration on tiny inputs, a library
+routine the step reduces to (matmul, stable sort, softmax, bincount), or a
+figure printed on the pages. A plausible slip in the oracle (a transposed
+weight, a missing renormalisation, a wrong tie rule, an unstable permutation,
+a wrong activation) fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import special
+
+import oracle
+from moe_synth import f32_to_bf16_bits, bf16_bits_to_f32
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+GOLD = json.load(open(os.path.join(HERE, "golden", "pages_figures.json")))
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# ---------------------------------------------------------------- gate / route
+def test_gate_logits_equal_matmul():
+    """logits = x @ W_g (+ b): the pages' gate projection is a plain matmul."""
+    x = _rand((37, 24), 1)
+    wg = _rand((24, 7), 2, 0.3)
+    b = _rand((7,), 3)
+    r = oracle.route(x, wg, 3, bias=b, want_logits=True)
+    ref = x @ wg + b
+    np.testing.assert_allclose(r["logits"], ref, rtol=1e-12, atol=1e-12)
+    # and the transpose would differ: guards the [d, N] layout reading
+    assert not np.allclose(r["logits"][:, :7], (x[:, :7] @ wg[:7, :7].T) + b)
+
+
+def test_gate_reads_fp32_and_bf16_inputs_exactly():
+    x32 = _rand((5, 16), 4).astype(np.float32)
+    xb = f32_to_bf16_bits(x32)
+    wg = _rand((16, 4), 5, 0.1).astype(np.float32)
+    r32 = oracle.route(x32, wg, 2, want_logits=True)
+    rb = oracle.route(xb, wg, 2, want_logits=True)
+    np.testing.assert_allclose(r32["logits"], x32.astype(np.float64) @ wg.astype(np.float64), rtol=1e-13)
+    np.testing.assert_allclose(rb["logits"],
+                               bf16_bits_to_f32(xb).astype(np.float64) @ wg.astype(np.float64), rtol=1e-13)
+
+
+@pytest.mark.parametrize("N,k", [(5, 1), (5, 2), (6, 3), (7, 4), (6, 6)])
+def test_topk_is_bruteforce_best_subset(N, k):
+    """Top-k = the k-subset with the largest total score (brute force over all
+    subsets), listed in descending score order."""
+    T, d = 40, 9
+    x = _rand((T, d), 10 + N)
+    wg = _rand((d, N), 20 + k)
+    b = _rand((N,), 30)
+    r = oracle.route(x, wg, k, bias=b)
+    L = x @ wg + b
+    for t in range(T):
+        best = max(itertools.combinations(range(N), k), key=lambda s: sum(L[t, list(s)]))
+        got = r["topk_idx"][t]
+        assert sorted(got.tolist()) == sorted(best)
+        assert all(L[t, got[j]] > L[t, got[j + 1]] for j in range(k - 1))
+
+
+def test_topk_tie_rule_lower_id_wins():
+    """Exact ties (integer data): the lower expert id is selected and listed first."""
+    x = np.array([[1.0]])
+    wg = np.array([[2.0, 5.0, 5.0, 1.0, 5.0]])
+    r = oracle.route(x, wg, 1)
+    assert r["topk_idx"].tolist() == [[1]]
+    r = oracle.route(x, wg, 2)
+    assert r["topk_idx"].tolist() == [[1, 2]]
+    r = oracle.route(x, wg, 4)
+    assert r["topk_idx"].tolist() == [[1, 2, 4, 0]]
+    np.testing.assert_allclose(r["topk_w"].sum(), 1.0, rtol=1e-15)
+    # a tie is never certified
+    assert r["cert"][0] <= 0
+
+
+def test_renormalised_weights_sum_to_one_and_follow_softmax_ratios():
+    """g_i' = g_i / sum_sel g: weights sum to 1, and w_a / w_b = p_a / p_b =
+    exp(l_a - l_b) because the softmax is proportional to exp(logit)."""
+    x = _rand((64, 12), 40)
+    wg = _rand((12, 9), 41)
+    for k in (1, 2, 3, 5, 9):
+        r = oracle.route(x, wg, k, want_logits=True)
+        w, idx, L = r["topk_w"], r["topk_idx"], r["logits"]
+        np.testing.assert_allclose(w.sum(1), 1.0, rtol=0, atol=1e-12)
+        if k == 1:
+            np.testing.assert_allclose(w, 1.0, atol=1e-15)
+        for t in range(0, 64, 7):
+            for a, b in itertools.combinations(range(k), 2):
+                np.testing.assert_allclose(w[t, a] / w[t, b], math.exp(L[t, idx[t, a]] - L[t, idx[t, b]]),
+                                           rtol=1e-12)
+
+
+def test_k_equals_n_weights_are_the_full_softmax():
+    """With k = N nothing is dropped, so the renormalised weights are the
+    softmax over all experts (scipy's softmax as the library routine)."""
+    x = _rand((20, 8), 50)
+    wg = _rand((8, 6), 51)
+    b = _rand((6,), 52)
+    r = oracle.route(x, wg, 6, bias=b)
+    P = special.softmax(x @ wg + b, axis=1)
+    for t in range(20):
+        np.testing.assert_allclose(r["topk_w"][t], P[t, r["topk_idx"][t]], rtol=1e-12)
+
+
+def test_token_A_printed_example():
+    """Token A on experts 0 and 3 with probabilities 0.7 / 0.3 combines as
+    0.7 * E0 + 0.3 * E3 (pages' printed example). Build logits ln 0.7, ln 0.3
+    with the other experts far below, d = F = 1 experts with closed forms."""
+    g = GOLD["worked_example"]["token_A"]
+    x = np.array([[1.0]])
+    wg = np.array([[math.log(0.7), -40.0, -40.0, math.log(0.3)]])
+    r = oracle.route(x, wg, 2)
+    assert r["topk_idx"].tolist() == [g["experts"]]
+    np.testing.assert_allclose(r["topk_w"][0], g["probs"], rtol=1e-12)
+    # SwiGLU experts with d = F = 1: y = c * silu(a x) * (b x)
+    a = np.array([0.5, 1.0, -1.0, 2.0]); bb = np.array([1.5, 1.0, 1.0, -0.5]); c = np.array([2.0, 1.0, 1.0, 3.0])
+    WG = a.reshape(4, 1, 1); WU = bb.reshape(4, 1, 1); WD = c.reshape(4, 1, 1)
+    f = oracle.forward(x, wg, None, WG, WU, WD, 2, "swiglu")
+    def E(e):
+        v = a[e]
+        return c[e] * (v / (1 + math.exp(-v))) * bb[e]
+    np.testing.assert_allclose(f["out"][0, 0], 0.7 * E(0) + 0.3 * E(3), rtol=1e-12)
+
+
+def test_error_bound_covers_fp32_evaluations():
+    """errb bounds |fl32(l) - l| for any summation order: check against fp32
+    sums taken sequentially, reversed, pairwise (numpy) and with a bias add."""
+    rng = np.random.default_rng(60)
+    T, d, N = 16, 512, 8
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = (0.02 * rng.standard_normal((d, N))).astype(np.float32)
+    b = rng.standard_normal(N).astype(np.float32)
+    r = oracle.route(x, wg, 2, bias=b, want_logits=True)
+    prods = x[:, :, None] * wg[None, :, :]               # fp32 products [T, d, N]
+    seq = np.zeros((T, N), np.float32)
+    for i in range(d):
+        seq = seq + prods[:, i, :]
+    rev = np.zeros((T, N), np.float32)
+    for i in reversed(range(d)):
+        rev = rev + prods[:, i, :]
+    pair = prods.sum(axis=1, dtype=np.float32)
+    for s32 in (seq, rev, pair):
+        l32 = (s32 + b).astype(np.float64)
+        assert np.all(np.abs(l32 - r["logits"]) <= r["errb"])
+    assert np.all(r["errb"] > 0)
+    # the bound is not vacuous: within ~1e3 ulps of the logit scale
+    assert np.all(r["errb"] < 1e-3)
+
+
+def test_cert_positive_on_continuous_data():
+    x = _rand((200, 64), 70).astype(np.float32)
+    wg = (0.02 * _rand((64, 16), 71)).astype(np.float32)
+    r = oracle.route(x, wg, 4)
+    assert (r["cert"] > 0).mean() > 0.95
+
+
+# ---------------------------------------------------------------- permutation
+def _random_routing(T, N, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.choice(N, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,N,k", [(1, 1, 1), (33, 5, 2), (100, 8, 8), (257, 16, 3)])
+def test_permute_matches_stable_sort(T, N, k):
+    """counts = bincount, offsets = cumsum with offsets[N] = T*k (the pages'
+    sum N_i = B*S*k), rows = a stable sort of the flat assignments by expert."""
+    idx = _random_routing(T, N, k, T + N)
+    p = oracle.permute(idx, N)
+    flat = idx.reshape(-1)
+    np.testing.assert_array_equal(p["counts"], np.bincount(flat, minlength=N))
+    assert p["counts"].sum() == T * k
+    np.testing.assert_array_equal(p["offsets"], np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=N))]))
+    order = np.argsort(flat, kind="stable")            # row -> flat assignment
+    np.testing.assert_array_equal(p["perm"], order // k)
+    inv = np.empty_like(order)
+    inv[order] = np.arange(T * k)
+    np.testing.assert_array_equal(p["inv_perm"], inv)
+    # bijection and round trip
+    assert sorted(p["inv_perm"].tolist()) == list(range(T * k))
+    np.testing.assert_array_equal(p["perm"][p["inv_perm"]], np.arange(T * k) // k)
+
+
+def test_permute_empty_experts_and_all_on_one():
+    idx = np.full((10, 1), 3, np.int32)
+    p = oracle.permute(idx, 6)
+    assert p["counts"].tolist() == [0, 0, 0, 10, 0, 0]
+    assert p["offsets"].tolist() == [0, 0, 0, 0, 10, 10, 10]
+    assert p["perm"].tolist() == list(range(10))
+
+
+def test_permute_rejects_bad_index():
+    with pytest.raises(ValueError):
+        oracle.permute(np.array([[0, 7]], np.int32), 4)
+
+
+def test_worked_example_assignment_total():
+    """[4, 2048] tokens, 64 experts, top-2: the N_i sum to 16,384 and the
+    top-k tensors have 16,384 elements (printed)."""
+    g = GOLD["worked_example"]
+    T = g["batch"] * g["seq"]
+    idx = _random_routing(T, g["experts"], g["top_k"], 80)
+    p = oracle.permute(idx, g["experts"])
+    assert int(p["counts"].sum()) == g["assignments_total"] == idx.size == g["topk_elements"]
+    assert T * g["experts"] == g["logits_elements"]
+    assert g["logits_elements"] * 2 == g["logits_bytes_fp16"]
+    assert g["topk_elements"] * (4 + 2) == g["topk_bytes_int32_plus_fp16"]
+
+
+# ---------------------------------------------------------------- expert FFN
+def test_activation_closed_forms():
+    """d = F = 1 experts: SwiGLU y = c * silu(a x) * (b x) with silu(v) =
+    v * sigmoid(v) (scipy's expit); GELU y = c * gelu_tanh(a x) with the
+    textbook tanh form; both checked at several points."""
+    for xv in (-3.0, -0.7, 0.0, 0.4, 2.5):
+        x = np.array([[xv]])
+        a, b, c = 0.9, -1.3, 1.7
+        y = oracle.expert_rows(x, np.array([[a]]), np.array([[b]]), np.array([[c]]), "swiglu")
+        v = a * xv
+        np.testing.assert_allclose(y[0, 0], c * v * special.expit(v) * (b * xv), rtol=1e-13, atol=1e-300)
+        y = oracle.expert_rows(x, np.array([[a]]), None, np.array([[c]]), "gelu_tanh")
+        ref = c * 0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+        np.testing.assert_allclose(y[0, 0], ref, rtol=1e-13, atol=1e-300)
+
+
+def test_gelu_tanh_is_close_to_exact_gelu():
+    """The tanh form approximates GELU(v) = v * Phi(v) (scipy's ndtr) to a few
+    1e-4: pins that the oracle uses a GELU, not another activation."""
+    v = np.linspace(-6, 6, 241)
+    y = np.array([oracle.expert_rows(np.array([[t]]), np.array([[1.0]]), None, np.array([[1.0]]),
+                                     "gelu_tanh")[0, 0] for t in v])
+    assert np.max(np.abs(y - v * special.ndtr(v))) < 1e-3
+    assert abs(y[np.argmin(np.abs(v - 1.0))] - 0.8411919906082768) < 1e-12
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu_tanh"])
+def test_expert_rows_equal_matmul_form(act):
+    """Row-by-row loops equal the batched matrix form of the same FFN built
+    from library matmuls: y = W_down (act(W_gate X^T) [* W_up X^T])."""
+    rng = np.random.default_rng(90)
+    n, d, F = 6, 10, 14
+    X = rng.standard_normal((n, d))
+    Wg = rng.standard_normal((F, d)) * 0.3
+    Wu = rng.standard_normal((F, d)) * 0.3 if act == "swiglu" else None
+    Wd = rng.standard_normal((d, F)) * 0.3
+    y, h = oracle.expert_rows(X, Wg, Wu, Wd, act, want_h=True)
+    G = X @ Wg.T
+    if act == "swiglu":
+        H = G * special.expit(G) * (X @ Wu.T)
+    else:
+        H = 0.5 * G * (1 + np.tanh(math.sqrt(2 / math.pi) * (G + 0.044715 * G ** 3)))
+    np.testing.assert_allclose(h, H, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(y, H @ Wd.T, rtol=1e-11, atol=1e-13)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu_tanh"])
+def test_identical_experts_give_dense_ffn(act):
+    """All experts equal => for any routing the layer is one dense FFN, since
+    the renormalised weights sum to 1 (pages: weighted sum of expert outputs)."""
+    rng = np.random.default_rng(100)
+    T, d, N, k, F = 23, 12, 5, 3, 16
+    x = rng.standard_normal((T, d))
+    wg = rng.standard_normal((d, N))
+    Wg1 = rng.standard_normal((F, d)) * 0.2
+    Wu1 = rng.standard_normal((F, d)) * 0.2
+    Wd1 = rng.standard_normal((d, F)) * 0.2
+    WG = np.repeat(Wg1[None], N, 0)
+    WU = np.repeat(Wu1[None], N, 0) if act == "swiglu" else None
+    WD = np.repeat(Wd1[None], N, 0)
+    f = oracle.forward(x, wg, None, WG, WU, WD, k, act)
+    G = x @ Wg1.T
+    H = G * special.expit(G) * (x @ Wu1.T) if act == "swiglu" else \
+        0.5 * G * (1 + np.tanh(math.sqrt(2 / math.pi) * (G + 0.044715 * G ** 3)))
+    np.testing.assert_allclose(f["out"], H @ Wd1.T, rtol=1e-10, atol=1e-12)
+
+
+def test_k_equals_n_is_the_full_softmax_mixture():
+    """k = N: out = sum_n softmax(l)_n * E_n(x), computed without any routing."""
+    rng = np.random.default_rng(110)
+    T, d, N, F = 9, 8, 4, 6
+    x = rng.standard_normal((T, d))
+    wg = rng.standard_normal((d, N))
+    b = rng.standard_normal(N)
+    WG = rng.standard_normal((N, F, d)) * 0.3
+    WU = rng.standard_normal((N, F, d)) * 0.3
+    WD = rng.standard_normal((N, d, F)) * 0.3
+    f = oracle.forward(x, wg, b, WG, WU, WD, N, "swiglu")
+    P = special.softmax(x @ wg + b, axis=1)
+    ref = np.zeros((T, d))
+    for n in range(N):
+        G = x @ WG[n].T
+        ref += P[:, n:n + 1] * ((G * special.expit(G) * (x @ WU[n].T)) @ WD[n].T)
+    np.testing.assert_allclose(f["out"], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_forward_bruteforce_per_token_loop():
+    """Tiny case (2 x 8 tokens, d 16, 4 experts, top-2 -- the shapes of the
+    pages' toy forward): each output row equals the per-token definition
+    sum_j w_j E_{e_j}(x_t) with experts from library matmuls, and the
+    permuted rows hold x of the right token."""
+    rng = np.random.default_rng(120)
+    T, d, N, k, F = 16, 16, 4, 2, 24
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = (rng.standard_normal((d, N)) * 0.5).astype(np.float32)
+    WG = rng.standard_normal((N, F, d)) * 0.2
+    WU = rng.standard_normal((N, F, d)) * 0.2
+    WD = rng.standard_normal((N, d, F)) * 0.2
+    f = oracle.forward(x, wg, None, WG, WU, WD, k, "swiglu")
+    L = x.astype(np.float64) @ wg.astype(np.float64)
+    for t in range(T):
+        sel = sorted(range(N), key=lambda n: (-L[t, n], n))[:k]
+        p = special.softmax(L[t])[sel]
+        p = p / p.sum()
+        ref = np.zeros(d)
+        for j, e in enumerate(sel):
+            G = WG[e] @ x[t]
+            ref += p[j] * (WD[e] @ (G * special.expit(G) * (WU[e] @ x[t])))
+        np.testing.assert_allclose(f["out"][t], ref, rtol=1e-10, atol=1e-12)
+        for j in range(k):
+            assert f["perm"][f["inv_perm"][t * k + j]] == t
+
+
+def test_combine_one_hot_and_order():
+    y = np.arange(12, dtype=np.float64).reshape(4, 3)
+    inv = np.array([2, 0, 3, 1], np.int32)     # T=2, k=2
+    w = np.array([[1.0, 0.0], [0.25, 0.75]])
+    out = oracle.combine(y, inv, w)
+    np.testing.assert_allclose(out[0], y[2])
+    np.testing.assert_allclose(out[1], 0.25 * y[3] + 0.75 * y[1])
+    out = oracle.combine(y, inv, w, tokens=[1])
+    np.testing.assert_allclose(out[0], 0.25 * y[3] + 0.75 * y[1])

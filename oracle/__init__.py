@@ -1,4 +1,10 @@
-"""CPU fp64 oracle of the MoE layer forward -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle of the MoE layer forward -- TEST INFRASTRUCTURE ONLY.
+
+Everything is computed in fp64 except the gate logits, which the pages keep in
+fp32 ("MoE混合专家模型计算原理与推理部署实战解析" sections 2.4 and 7): the top-k
+decision is taken on the plain fp32 evaluation of x @ W_g (a sequential FMA
+chain in index order), so that an fp32 kernel can be held to bit-exact
+routing. gate="fp64" gives the exact-logit decision for comparison.
 
 Only the tests, the package smoke check and the benchmark's CPU baseline may
 import this package. The CUDA library never links, loads or calls it, and it
@@ -34,7 +40,7 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (-O2, OpenMP). Returns the .so path."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c99",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
@@ -47,7 +53,7 @@ def lib():
         L = ctypes.CDLL(_LIB)
         P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.oracle_num_threads.restype = I
-        L.oracle_route.argtypes = [I64, I, I, I, P, I, P, I, P, I, P, P, P, P, P]
+        L.oracle_route.argtypes = [I64, I, I, I, P, I, P, I, P, I, I, P, P, P, P, P]
         L.oracle_route.restype = I
         L.oracle_permute.argtypes = [I64, I, I, P, P, P, P, P]
         L.oracle_permute.restype = I
@@ -55,7 +61,7 @@ def lib():
         L.oracle_expert_rows.restype = I
         L.oracle_combine.argtypes = [I64, P, I, I, P, P, P, P]
         L.oracle_combine.restype = I
-        L.oracle_forward.argtypes = [I64, I, I, I, I, I, P, I, P, I, P, I, P, P, P, I,
+        L.oracle_forward.argtypes = [I64, I, I, I, I, I, P, I, P, I, P, I, I, P, P, P, I,
                                      P, P, P, P, P, P, P, P, P]
         L.oracle_forward.restype = I
         _lib = L
@@ -86,11 +92,13 @@ def _p(a):
     return None if a is None else a.ctypes.data
 
 
-def route(x, wg, k, bias=None, want_logits=False):
+def route(x, wg, k, bias=None, want_logits=False, gate="fp32"):
     """Gate -> softmax -> top-k -> renormalise for every row of x.
 
-    Returns dict(topk_idx [T,k] int32, topk_w [T,k] f64, cert [T] f64,
-    errb [T,N] f64, and logits [T,N] f64 when asked)."""
+    gate="fp32" (the pages' precision for the gate) takes the top-k decision
+    on the fp32 logits of the sequential FMA chain; gate="fp64" on exact
+    logits. Returns dict(topk_idx [T,k] int32, topk_w [T,k] f64, cert [T],
+    errb [T,N] (both about the exact logits), and logits [T,N] when asked)."""
     x, wg, bias = _c(x), _c(wg), _c(bias)
     T, d = x.shape
     N = wg.shape[1]
@@ -100,7 +108,7 @@ def route(x, wg, k, bias=None, want_logits=False):
     errb = np.empty((T, N), np.float64)
     logits = np.empty((T, N), np.float64) if want_logits else None
     rc = lib().oracle_route(T, d, N, k, _p(x), _dt(x), _p(wg), _dt(wg), _p(bias), _dt(bias),
-                            _p(idx), _p(w), _p(logits), _p(errb), _p(cert))
+                            1 if gate == "fp32" else 0, _p(idx), _p(w), _p(logits), _p(errb), _p(cert))
     if rc:
         raise ValueError("oracle_route: bad arguments")
     out = dict(topk_idx=idx, topk_w=w, cert=cert, errb=errb)
@@ -152,7 +160,7 @@ def combine(y_perm, inv_perm, topk_w, tokens=None):
     return out
 
 
-def forward(x, wg, bias, w_gate, w_up, w_down, k, act):
+def forward(x, wg, bias, w_gate, w_up, w_down, k, act, gate="fp32"):
     """The whole layer: route -> permute -> per-expert FFN -> combine."""
     x, wg, bias, w_gate, w_up, w_down = map(_c, (x, wg, bias, w_gate, w_up, w_down))
     T, d = x.shape
@@ -165,7 +173,7 @@ def forward(x, wg, bias, w_gate, w_up, w_down, k, act):
              inv_perm=np.empty(A, np.int32), y_perm=np.empty((A, d), np.float64),
              out=np.empty((T, d), np.float64))
     rc = lib().oracle_forward(T, d, N, k, F, ACTS[act], _p(x), _dt(x), _p(wg), _dt(wg), _p(bias), _dt(bias),
-                              _p(w_gate), _p(w_up), _p(w_down), _dt(w_gate),
+                              1 if gate == "fp32" else 0, _p(w_gate), _p(w_up), _p(w_down), _dt(w_gate),
                               _p(r["topk_idx"]), _p(r["topk_w"]), _p(r["cert"]), _p(r["counts"]),
                               _p(r["offsets"]), _p(r["perm"]), _p(r["inv_perm"]), _p(r["y_perm"]),
                               _p(r["out"]))

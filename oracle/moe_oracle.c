@@ -1,12 +1,13 @@
 /*
- * moe_oracle.c -- CPU fp64 oracle of the MoE layer forward.
+ * moe_oracle.c -- CPU oracle of the MoE layer forward (fp64; fp32 gate).
  *
  * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call
  * this file: only the tests, the package's smoke check and the benchmark's CPU
  * baseline use it. It shares no code, header or table with the CUDA library.
  *
  * It is a plain, slow, obviously correct restatement of what the pages define,
- * in double precision end to end. Inputs are read exactly as the GPU receives
+ * in double precision except for the gate logits, which the pages keep in
+ * fp32 (see the readings below). Inputs are read exactly as the GPU receives
  * them (fp32 or bf16 values widened to fp64, which is exact). OpenMP only
  * splits independent tokens / rows across host threads.
  *
@@ -23,6 +24,12 @@
  *        per-expert GEMM -> unpermute + weighted merge.
  *
  * Readings where the pages are silent (each is listed in the design notes):
+ *   - the gate is computed in fp32 ([P3] s2.4 and s7 keep the gate in FP32
+ *     and the experts in bf16). Its plainest fp32 evaluation is used: for
+ *     each logit the sequential chain s <- fma(x_i, W_g[i,n], s) over
+ *     i = 0..d-1 from s = 0, then one fp32 addition of the bias. The top-k
+ *     decision is taken on these fp32 values; softmax and renormalisation
+ *     then run in fp64 on them. (gate_fp32 = 0 gives exact fp64 logits.)
  *   - top-k is taken on the score s = logit (+ per-expert bias); softmax is
  *     monotone, so this is the pages' top-k over probabilities, without the
  *     false ties that rounded probabilities can create;
@@ -65,29 +72,31 @@ int oracle_num_threads(void)
 }
 
 /* ---------------------------------------------------------------------------
- * Route: [P2] s2.1-2.2, [P3] s2.1-2.2.
- *   l[t,n] = sum_i x[t,i] * W_g[i,n] (+ b[n])
+ * Route: [P2] s2.1-2.2, [P3] s2.1-2.2, s2.4.
+ *   l[t,n] = sum_i x[t,i] * W_g[i,n] (+ b[n])   in fp32 when gate_fp32 != 0
+ *            (sequential FMA chain in index order, then + b in fp32),
+ *            else exactly in fp64
  *   p[t,:] = softmax(l[t,:])
  *   top-k by l (ties -> lower id), in descending order
  *   w[t,j] = p[t,e_j] / sum_j' p[t,e_j']
  *
- * Also returns, per token, what a parity test needs to judge an fp32
- * evaluation of the same logits:
- *   errb[t,n]  a bound on |fl32(l[t,n]) - l[t,n]| for ANY summation order:
+ * Also returns, per token, how fragile the decision is against rounding
+ * (computed from the exact fp64 logits whatever gate_fp32 says):
+ *   errb[t,n]  a bound on |fl32(l[t,n]) - l_exact[t,n]| for ANY fp32 summation order:
  *              gamma_{d+2} * (sum_i |x_i W_g[i,n]| + |b_n|), gamma_m = m u/(1-m u),
  *              u = 2^-24 (the classical bound for a sum of d rounded products
  *              plus one rounded bias addition);
- *   cert[t]    min over i < k, j > i (sorted order) of
- *              (l_(i) - errb_(i)) - (l_(j) + errb_(j)).
- *              cert > 0 proves that an fp32 evaluation selects the same experts
- *              in the same order.
- *   logits     optional [T,N] copy of l.
+ *   cert[t]    min over i < k, j > i (sorted exact order) of
+ *              (l_(i) - errb_(i)) - (l_(j) + errb_(j)) on the exact logits.
+ *              cert > 0 proves that ANY fp32 evaluation selects the same
+ *              experts in the same order as exact arithmetic.
+ *   logits     optional [T,N] copy of l (the fp32 values when gate_fp32).
  * Returns 0, or -1 on bad arguments.
  * ------------------------------------------------------------------------- */
 int oracle_route(int64_t T, int d, int N, int k,
                  const void *x, int x_dt,
                  const void *wg, int wg_dt,
-                 const void *bias, int b_dt,
+                 const void *bias, int b_dt, int gate_fp32,
                  int32_t *topk_idx, double *topk_w,
                  double *logits, double *errb, double *cert)
 {
@@ -102,9 +111,10 @@ int oracle_route(int64_t T, int d, int N, int k,
         double *s = (double *)malloc(sizeof(double) * N);
         double *p = (double *)malloc(sizeof(double) * N);
         double *eb = (double *)malloc(sizeof(double) * N);
+        double *ex = (double *)malloc(sizeof(double) * N);
         int *taken = (int *)malloc(sizeof(int) * N);
         int *order = (int *)malloc(sizeof(int) * N);
-        if (!l || !s || !p || !eb || !taken || !order) {
+        if (!l || !s || !p || !eb || !ex || !taken || !order) {
 #pragma omp atomic write
             bad = 1;
         } else {
@@ -113,13 +123,17 @@ int oracle_route(int64_t T, int d, int N, int k,
                 /* gate projection */
                 for (int n = 0; n < N; ++n) {
                     double acc = 0.0, aabs = 0.0;
+                    float acc32 = 0.0f;
                     for (int i = 0; i < d; ++i) {
-                        double prod = rd(x, x_dt, t * d + i) * rd(wg, wg_dt, (int64_t)i * N + n);
+                        double xi = rd(x, x_dt, t * d + i), wi = rd(wg, wg_dt, (int64_t)i * N + n);
+                        double prod = xi * wi;
                         acc += prod;
                         aabs += fabs(prod);
+                        if (gate_fp32) acc32 = fmaf((float)xi, (float)wi, acc32);
                     }
                     double b = bias ? rd(bias, b_dt, n) : 0.0;
-                    l[n] = acc + b;
+                    ex[n] = acc + b;
+                    l[n] = gate_fp32 ? (double)(bias ? acc32 + (float)b : acc32) : acc + b;
                     s[n] = aabs + fabs(b);
                     eb[n] = gam * s[n];
                 }
@@ -150,11 +164,22 @@ int oracle_route(int64_t T, int d, int N, int k,
                 if (logits) for (int n = 0; n < N; ++n) logits[t * N + n] = l[n];
                 if (errb) for (int n = 0; n < N; ++n) errb[t * N + n] = eb[n];
                 if (cert) {
+                    /* order of the exact logits, then the smallest separation */
+                    for (int n = 0; n < N; ++n) taken[n] = 0;
+                    for (int r = 0; r < N; ++r) {
+                        int best = -1;
+                        for (int n = 0; n < N; ++n) {
+                            if (taken[n]) continue;
+                            if (best < 0 || ex[n] > ex[best]) best = n;
+                        }
+                        taken[best] = 1;
+                        order[r] = best;
+                    }
                     double c = INFINITY;
                     for (int i = 0; i < k; ++i) {
-                        double lo = l[order[i]] - eb[order[i]];
+                        double lo = ex[order[i]] - eb[order[i]];
                         for (int j2 = i + 1; j2 < N; ++j2) {
-                            double hi = l[order[j2]] + eb[order[j2]];
+                            double hi = ex[order[j2]] + eb[order[j2]];
                             if (lo - hi < c) c = lo - hi;
                         }
                     }
@@ -162,7 +187,7 @@ int oracle_route(int64_t T, int d, int N, int k,
                 }
             }
         }
-        free(l); free(s); free(p); free(eb); free(taken); free(order);
+        free(l); free(s); free(p); free(eb); free(ex); free(taken); free(order);
     }
     return bad ? -1 : 0;
 }
@@ -287,14 +312,14 @@ int oracle_combine(int64_t n_tok, const int64_t *tokens, int d, int k,
  * out [T, d] fp64. Routing outputs as in oracle_route / oracle_permute.
  * ------------------------------------------------------------------------- */
 int oracle_forward(int64_t T, int d, int N, int k, int F, int act,
-                   const void *x, int x_dt, const void *wg, int wg_dt, const void *bias, int b_dt,
+                   const void *x, int x_dt, const void *wg, int wg_dt, const void *bias, int b_dt, int gate_fp32,
                    const void *w_gate, const void *w_up, const void *w_down, int w_dt,
                    int32_t *topk_idx, double *topk_w, double *cert,
                    int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                    double *y_perm, double *out)
 {
     const int64_t A = T * k;
-    int rc = oracle_route(T, d, N, k, x, x_dt, wg, wg_dt, bias, b_dt, topk_idx, topk_w, NULL, NULL, cert);
+    int rc = oracle_route(T, d, N, k, x, x_dt, wg, wg_dt, bias, b_dt, gate_fp32, topk_idx, topk_w, NULL, NULL, cert);
     if (rc) return rc;
     rc = oracle_permute(T, N, k, topk_idx, counts, offsets, perm, inv_perm);
     if (rc) return rc;

@@ -33,7 +33,7 @@ def test_gate_logits_equal_matmul():
     x = _rand((37, 24), 1)
     wg = _rand((24, 7), 2, 0.3)
     b = _rand((7,), 3)
-    r = oracle.route(x, wg, 3, bias=b, want_logits=True)
+    r = oracle.route(x, wg, 3, bias=b, want_logits=True, gate="fp64")
     ref = x @ wg + b
     np.testing.assert_allclose(r["logits"], ref, rtol=1e-12, atol=1e-12)
     # and the transpose would differ: guards the [d, N] layout reading
@@ -44,8 +44,8 @@ def test_gate_reads_fp32_and_bf16_inputs_exactly():
     x32 = _rand((5, 16), 4).astype(np.float32)
     xb = f32_to_bf16_bits(x32)
     wg = _rand((16, 4), 5, 0.1).astype(np.float32)
-    r32 = oracle.route(x32, wg, 2, want_logits=True)
-    rb = oracle.route(xb, wg, 2, want_logits=True)
+    r32 = oracle.route(x32, wg, 2, want_logits=True, gate="fp64")
+    rb = oracle.route(xb, wg, 2, want_logits=True, gate="fp64")
     np.testing.assert_allclose(r32["logits"], x32.astype(np.float64) @ wg.astype(np.float64), rtol=1e-13)
     np.testing.assert_allclose(rb["logits"],
                                bf16_bits_to_f32(xb).astype(np.float64) @ wg.astype(np.float64), rtol=1e-13)
@@ -59,7 +59,7 @@ def test_topk_is_bruteforce_best_subset(N, k):
     x = _rand((T, d), 10 + N)
     wg = _rand((d, N), 20 + k)
     b = _rand((N,), 30)
-    r = oracle.route(x, wg, k, bias=b)
+    r = oracle.route(x, wg, k, bias=b, gate="fp64")
     L = x @ wg + b
     for t in range(T):
         best = max(itertools.combinations(range(N), k), key=lambda s: sum(L[t, list(s)]))
@@ -106,7 +106,7 @@ def test_k_equals_n_weights_are_the_full_softmax():
     x = _rand((20, 8), 50)
     wg = _rand((8, 6), 51)
     b = _rand((6,), 52)
-    r = oracle.route(x, wg, 6, bias=b)
+    r = oracle.route(x, wg, 6, bias=b, gate="fp64")
     P = special.softmax(x @ wg + b, axis=1)
     for t in range(20):
         np.testing.assert_allclose(r["topk_w"][t], P[t, r["topk_idx"][t]], rtol=1e-12)
@@ -119,13 +119,13 @@ def test_token_A_printed_example():
     g = GOLD["worked_example"]["token_A"]
     x = np.array([[1.0]])
     wg = np.array([[math.log(0.7), -40.0, -40.0, math.log(0.3)]])
-    r = oracle.route(x, wg, 2)
+    r = oracle.route(x, wg, 2, gate="fp64")
     assert r["topk_idx"].tolist() == [g["experts"]]
     np.testing.assert_allclose(r["topk_w"][0], g["probs"], rtol=1e-12)
     # SwiGLU experts with d = F = 1: y = c * silu(a x) * (b x)
     a = np.array([0.5, 1.0, -1.0, 2.0]); bb = np.array([1.5, 1.0, 1.0, -0.5]); c = np.array([2.0, 1.0, 1.0, 3.0])
     WG = a.reshape(4, 1, 1); WU = bb.reshape(4, 1, 1); WD = c.reshape(4, 1, 1)
-    f = oracle.forward(x, wg, None, WG, WU, WD, 2, "swiglu")
+    f = oracle.forward(x, wg, None, WG, WU, WD, 2, "swiglu", gate="fp64")
     def E(e):
         v = a[e]
         return c[e] * (v / (1 + math.exp(-v))) * bb[e]
@@ -140,7 +140,8 @@ def test_error_bound_covers_fp32_evaluations():
     x = rng.standard_normal((T, d)).astype(np.float32)
     wg = (0.02 * rng.standard_normal((d, N))).astype(np.float32)
     b = rng.standard_normal(N).astype(np.float32)
-    r = oracle.route(x, wg, 2, bias=b, want_logits=True)
+    r = oracle.route(x, wg, 2, bias=b, want_logits=True, gate="fp64")
+    r32 = oracle.route(x, wg, 2, bias=b, want_logits=True)
     prods = x[:, :, None] * wg[None, :, :]               # fp32 products [T, d, N]
     seq = np.zeros((T, N), np.float32)
     for i in range(d):
@@ -152,6 +153,7 @@ def test_error_bound_covers_fp32_evaluations():
     for s32 in (seq, rev, pair):
         l32 = (s32 + b).astype(np.float64)
         assert np.all(np.abs(l32 - r["logits"]) <= r["errb"])
+    assert np.all(np.abs(r32["logits"] - r["logits"]) <= r["errb"])
     assert np.all(r["errb"] > 0)
     # the bound is not vacuous: within ~1e3 ulps of the logit scale
     assert np.all(r["errb"] < 1e-3)
@@ -162,6 +164,12 @@ def test_cert_positive_on_continuous_data():
     wg = (0.02 * _rand((64, 16), 71)).astype(np.float32)
     r = oracle.route(x, wg, 4)
     assert (r["cert"] > 0).mean() > 0.95
+    # a bias with gaps of 10 separates the experts: the certificate (about the
+    # exact logits, bias included) is close to the gap
+    b = (10.0 * np.arange(16)).astype(np.float32)
+    r = oracle.route(0.01 * x, wg, 4, bias=b)
+    assert np.all(r["cert"] > 9.0)
+    assert r["topk_idx"].tolist() == [[15, 14, 13, 12]] * 200
 
 
 # ---------------------------------------------------------------- permutation
@@ -276,7 +284,7 @@ def test_identical_experts_give_dense_ffn(act):
     WG = np.repeat(Wg1[None], N, 0)
     WU = np.repeat(Wu1[None], N, 0) if act == "swiglu" else None
     WD = np.repeat(Wd1[None], N, 0)
-    f = oracle.forward(x, wg, None, WG, WU, WD, k, act)
+    f = oracle.forward(x, wg, None, WG, WU, WD, k, act, gate="fp64")
     G = x @ Wg1.T
     H = G * special.expit(G) * (x @ Wu1.T) if act == "swiglu" else \
         0.5 * G * (1 + np.tanh(math.sqrt(2 / math.pi) * (G + 0.044715 * G ** 3)))
@@ -293,7 +301,7 @@ def test_k_equals_n_is_the_full_softmax_mixture():
     WG = rng.standard_normal((N, F, d)) * 0.3
     WU = rng.standard_normal((N, F, d)) * 0.3
     WD = rng.standard_normal((N, d, F)) * 0.3
-    f = oracle.forward(x, wg, b, WG, WU, WD, N, "swiglu")
+    f = oracle.forward(x, wg, b, WG, WU, WD, N, "swiglu", gate="fp64")
     P = special.softmax(x @ wg + b, axis=1)
     ref = np.zeros((T, d))
     for n in range(N):
@@ -314,7 +322,7 @@ def test_forward_bruteforce_per_token_loop():
     WG = rng.standard_normal((N, F, d)) * 0.2
     WU = rng.standard_normal((N, F, d)) * 0.2
     WD = rng.standard_normal((N, d, F)) * 0.2
-    f = oracle.forward(x, wg, None, WG, WU, WD, k, "swiglu")
+    f = oracle.forward(x, wg, None, WG, WU, WD, k, "swiglu", gate="fp64")
     L = x.astype(np.float64) @ wg.astype(np.float64)
     for t in range(T):
         sel = sorted(range(N), key=lambda n: (-L[t, n], n))[:k]
@@ -338,3 +346,49 @@ def test_combine_one_hot_and_order():
     np.testing.assert_allclose(out[1], 0.25 * y[3] + 0.75 * y[1])
     out = oracle.combine(y, inv, w, tokens=[1])
     np.testing.assert_allclose(out[0], 0.25 * y[3] + 0.75 * y[1])
+
+
+# ---------------------------------------------------------------- fp32 gate
+def _round_f32(q):
+    """Round an exact rational to the nearest fp32, ties to even."""
+    from fractions import Fraction
+    c0 = np.float32(float(q))
+    cands = [c0, np.nextafter(c0, np.float32(np.inf)), np.nextafter(c0, np.float32(-np.inf))]
+    best = min(cands, key=lambda c: (abs(Fraction(float(c)) - q), int(np.array(c).view(np.uint32)) & 1))
+    return np.float32(best)
+
+
+def test_fp32_gate_is_the_sequential_fma_chain():
+    """The pages keep the gate in FP32. The oracle's fp32 logit is, bit for
+    bit, s <- fl32(x_i * W_g[i,n] + s) (one rounding per step: an FMA) over
+    i = 0..d-1 from 0, then fl32(s + b) -- checked against exact rational
+    arithmetic rounded to fp32 by hand."""
+    from fractions import Fraction
+    rng = np.random.default_rng(130)
+    T, d, N = 4, 13, 3
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = (0.3 * rng.standard_normal((d, N))).astype(np.float32)
+    b = rng.standard_normal(N).astype(np.float32)
+    r = oracle.route(x, wg, 1, bias=b, want_logits=True)
+    for t in range(T):
+        for n in range(N):
+            s = np.float32(0.0)
+            for i in range(d):
+                s = _round_f32(Fraction(float(x[t, i])) * Fraction(float(wg[i, n])) + Fraction(float(s)))
+            s = np.float32(s + b[n])
+            assert np.float32(r["logits"][t, n]) == s and float(s) == r["logits"][t, n]
+
+
+def test_fp32_decisions_differ_from_exact_only_on_uncertified_tokens():
+    """Where rounding can change the top-k (cert <= 0) the fp32 and exact
+    decisions may differ; everywhere else they must agree."""
+    rng = np.random.default_rng(140)
+    x = rng.standard_normal((3000, 256)).astype(np.float32)
+    wg = (0.02 * rng.standard_normal((256, 64))).astype(np.float32)
+    for b in (None, rng.standard_normal(64).astype(np.float32)):
+        r32 = oracle.route(x, wg, 4, bias=b)
+        r64 = oracle.route(x, wg, 4, bias=b, gate="fp64")
+        same = np.all(r32["topk_idx"] == r64["topk_idx"], axis=1)
+        assert np.all(same[r64["cert"] > 0])
+        assert same.mean() > 0.99
+        np.testing.assert_array_equal(r32["cert"], r64["cert"])

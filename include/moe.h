@@ -1,0 +1,179 @@
+/*
+ * moe.h -- C ABI of libmoe_b300.so: the forward pass of one Mixture-of-Experts
+ * layer on one NVIDIA B300 (sm_103a).
+ *
+ * The layer, as the pages define it:
+ *   "MoE显存与计算开销四阶段手算指南" section 2 (four stages: gate projection,
+ *   routing, grouped expert computation, weighted combine) and
+ *   "MoE混合专家模型计算原理与推理部署实战解析" sections 2.1-2.2 (gate, softmax,
+ *   top-k, renormalised gates, weighted sum), 3.1 (SwiGLU expert) and 5.1
+ *   (count -> prefix sum -> permute -> grouped GEMM -> unpermute + merge).
+ *
+ * Conventions for every call:
+ *   - Tensors are dense, row-major and live in DEVICE memory owned by the
+ *     caller; pointers must be 16-byte aligned. The library never allocates
+ *     or frees device memory (scratch comes from the caller's workspace) and
+ *     never synchronises, except moe_get_error.
+ *   - All work is queued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns before it runs.
+ *   - Argument errors are detected on the host and return a status before
+ *     anything is launched. Launch failures return MOE_ERR_CUDA. Errors found
+ *     by the kernels (an expert index out of range, offsets that do not add
+ *     up, a device-side wait that ran out) are recorded in a per-device error
+ *     word and reported by moe_get_error; outputs are then undefined.
+ *   - Shapes: T tokens, d model dim, N experts, k experts per token, F = d_ff
+ *     expert hidden dim, A = T*k token-expert assignments.
+ *     1 <= k <= N <= 256, T >= 0, T*k < 2^31.
+ *     dtype MOE_BF16: activations and expert weights bf16, gate fp32;
+ *       needs d % 128 == 0, F % 64 == 0 (SwiGLU) or F % 128 == 0 (GELU).
+ *     dtype MOE_F32: everything fp32; needs d % 4 == 0.
+ *   - Weights are stored [out, in]: w_gate, w_up [N, F, d]; w_down [N, d, F]
+ *     (for the two-matrix GELU FFN w_gate holds W_1 and w_up is NULL).
+ *   - Results do not depend on the stream, the launch order or the run:
+ *     no floating-point atomics are used anywhere.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, k > N, negative size ... */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but not handled (e.g. d % 128 != 0 in bf16) */
+    MOE_ERR_WORKSPACE = 3,     /* ws_bytes smaller than the call needs */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out (kernel returned) */
+    MOE_ERR_CORRUPT = 6        /* expert index out of range or inconsistent offsets */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_SWIGLU = 0, MOE_GELU_TANH = 1 } moe_act;
+
+typedef struct {
+    int64_t T;      /* tokens */
+    int32_t d;      /* model dim */
+    int32_t N;      /* experts */
+    int32_t k;      /* experts per token */
+    int32_t d_ff;   /* expert hidden dim F */
+    int32_t act;    /* moe_act */
+    int32_t dtype;  /* moe_dtype */
+} moe_shape;
+
+/*
+ * Gate and routing: "MoE显存与计算开销四阶段手算指南" sections 2.1-2.2,
+ * "MoE混合专家模型计算原理与推理部署实战解析" sections 2.1, 2.2, 2.4.
+ *   s[t,n]   = sum_i x[t,i] * w_g[i,n] (+ bias[n])   fp32, FMA accumulation
+ *   topk_idx = the k experts of largest s, descending; equal s -> lower id first
+ *   topk_w   = softmax(s) restricted to the k selected and renormalised to sum 1
+ * x [T,d] (bf16 or fp32 per dtype), w_g [d,N] fp32, bias [N] fp32 or NULL
+ * (added to the logits before the softmax). Outputs topk_idx [T,k] int32,
+ * topk_w [T,k] fp32. Needs no workspace.
+ */
+moe_status moe_route(const moe_shape *s, const void *x, const float *w_g, const float *bias,
+                     int32_t *topk_idx, float *topk_w, void *stream);
+
+/*
+ * Grouping by expert: "MoE显存与计算开销四阶段手算指南" section 2.3,
+ * "MoE混合专家模型计算原理与推理部署实战解析" section 5.1 steps 2-3.
+ *   counts[n]  = number of assignments to expert n (sum = T*k)
+ *   offsets    = exclusive prefix sum of counts, offsets[N] = T*k   ([N+1])
+ *   rows offsets[n] .. offsets[n+1]-1 hold expert n's assignments in flat
+ *   order f = t*k + j (a stable counting sort):
+ *   perm[row] = t,  inv_perm[f] = row,  x_perm[row,:] = x[t,:]
+ * topk_idx [T,k]; x [T,d]; x_perm [T*k, d] (dtype of x). Bit-exact and
+ * deterministic. ws: at least moe_permute_workspace_size(s) bytes.
+ * An index outside [0,N) records MOE_ERR_CORRUPT.
+ */
+moe_status moe_permute(const moe_shape *s, const int32_t *topk_idx, const void *x,
+                       int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                       void *x_perm, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Every active expert's FFN as grouped GEMMs over the permuted rows:
+ * "MoE混合专家模型计算原理与推理部署实战解析" section 3.1 (SwiGLU:
+ * h = SiLU(x W_gate^T) * (x W_up^T), y = h W_down^T) and section 3.2;
+ * "MoE显存与计算开销四阶段手算指南" sections 2.3 and 4.3 (one launch over
+ * all experts, inputs contiguous, expert_offsets).
+ * For MOE_GELU_TANH: h = gelu_tanh(x W_1^T), y = h W_2^T (w_up = NULL).
+ * x_perm [A,d], offsets [N+1] (as from moe_permute), y_perm [A,d].
+ * bf16: tcgen05 tensor cores, fp32 accumulation in tensor memory, h rounded
+ * to bf16; f32: fp32 CUDA-core GEMM. ws: moe_grouped_ffn_workspace_size(s)
+ * bytes (holds h). Offsets that are not a monotone partition of [0, A)
+ * record MOE_ERR_CORRUPT and the GEMMs do nothing.
+ */
+moe_status moe_grouped_ffn(const moe_shape *s, const void *x_perm, const int32_t *offsets,
+                           const void *w_gate, const void *w_up, const void *w_down,
+                           void *y_perm, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Weighted combine back to token order: "MoE显存与计算开销四阶段手算指南"
+ * section 2.4, "MoE混合专家模型计算原理与推理部署实战解析" sections 2.2 and 5.1
+ * step 5:   out[t,:] = sum_{j<k} topk_w[t,j] * y_perm[inv_perm[t*k+j], :]
+ * summed in j order in fp32, written once per row (no zero-fill, no atomics).
+ * y_perm [A,d], inv_perm [A], topk_w [T,k] fp32, out [T,d] (dtype).
+ */
+moe_status moe_combine(const moe_shape *s, const void *y_perm, const int32_t *inv_perm,
+                       const float *topk_w, void *out, void *stream);
+
+/*
+ * The whole layer, "MoE混合专家模型计算原理与推理部署实战解析" section 6.1
+ * steps 1-5: moe_route -> moe_permute -> moe_grouped_ffn -> moe_combine on one
+ * stream, intermediates in ws (moe_workspace_size(s) bytes). topk_idx,
+ * topk_w and counts may be NULL (then they live in ws) or caller buffers
+ * that receive the routing.
+ */
+moe_status moe_forward(const moe_shape *s, const void *x, const float *w_g, const float *bias,
+                       const void *w_gate, const void *w_up, const void *w_down, void *out,
+                       int32_t *topk_idx, float *topk_w, int32_t *counts,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_forward with x and out in HOST memory (pinned memory makes the copies
+ * asynchronous): copies x into ws, runs the layer, copies out back, all on
+ * `stream`. The caller synchronises the stream before reading out_host.
+ * ws: moe_forward_hostio_workspace_size(s) bytes.
+ */
+moe_status moe_forward_hostio(const moe_shape *s, const void *x_host, const float *w_g,
+                              const float *bias, const void *w_gate, const void *w_up,
+                              const void *w_down, void *out_host, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* Workspace sizes in bytes (0 when the shape is invalid or unsupported). */
+size_t moe_workspace_size(const moe_shape *s);
+size_t moe_forward_hostio_workspace_size(const moe_shape *s);
+size_t moe_permute_workspace_size(const moe_shape *s);
+size_t moe_grouped_ffn_workspace_size(const moe_shape *s);
+
+/* Host-side shape check: MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED. */
+moe_status moe_check_shape(const moe_shape *s);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error
+ * word (MOE_OK if no kernel recorded an error). MOE_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+moe_status moe_get_error(void *stream);
+
+/*
+ * Self-test of the bounded device-side wait used by the pipelined kernels:
+ * one CTA waits on a shared-memory barrier that nothing ever completes,
+ * gives up after timeout_ns (clamped to [1 ms, 2 s]), records
+ * MOE_ERR_TIMEOUT and returns. The context stays usable.
+ */
+moe_status moe_selftest_bounded_wait(int64_t timeout_ns, void *stream);
+
+const char *moe_status_string(moe_status st);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

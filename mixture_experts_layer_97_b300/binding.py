@@ -1,0 +1,185 @@
+"""ctypes binding of libmoe_b300.so (the C ABI in include/moe.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the cudaStream_t, a non-OK status becomes ``MoEError``. Every
+step of the layer runs in the library's kernels. There is no CPU fallback:
+if the library is missing or a tensor is not on a CUDA device, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_b300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
+MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_CORRUPT = 4, 5, 6
+MOE_F32, MOE_BF16 = 0, 1
+MOE_SWIGLU, MOE_GELU_TANH = 0, 1
+ACT = {"swiglu": MOE_SWIGLU, "gelu_tanh": MOE_GELU_TANH}
+DTYPE = {"f32": MOE_F32, "bf16": MOE_BF16}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+# Every symbol the header declares, with its ctypes signature.
+P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("N", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("d_ff", ctypes.c_int32), ("act", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+SP = ctypes.POINTER(MoeShape)
+SIGNATURES = {
+    "moe_route": (I32, [SP, P, P, P, P, P, P]),
+    "moe_permute": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_grouped_ffn": (I32, [SP, P, P, P, P, P, P, P, SZ, P]),
+    "moe_combine": (I32, [SP, P, P, P, P, P]),
+    "moe_forward": (I32, [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_forward_hostio": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_workspace_size": (SZ, [SP]),
+    "moe_forward_hostio_workspace_size": (SZ, [SP]),
+    "moe_permute_workspace_size": (SZ, [SP]),
+    "moe_grouped_ffn_workspace_size": (SZ, [SP]),
+    "moe_check_shape": (I32, [SP]),
+    "moe_get_error": (I32, [P]),
+    "moe_selftest_bounded_wait": (I32, [I64, P]),
+    "moe_status_string": (ctypes.c_char_p, [I32]),
+    "moe_version": (ctypes.c_int, []),
+}
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib():
+    """Open the library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libmoe_b300.so is not built ({LIB_PATH}); run "
+                               "`python -m mixture_experts_layer_97_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return lib().moe_status_string(st).decode()
+
+
+def shape(T: int, d: int, N: int, k: int, F: int, act: str = "swiglu", dtype: str = "bf16") -> MoeShape:
+    return MoeShape(T, d, N, k, F, ACT[act], DTYPE[dtype])
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise RuntimeError("MoE library tensors must live on a CUDA device (there is no CPU path)")
+    if not t.is_contiguous():
+        raise RuntimeError("MoE library tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _host_ptr(t: torch.Tensor):
+    if t.is_cuda or not t.is_contiguous():
+        raise RuntimeError("host buffer expected (contiguous CPU tensor, ideally pinned)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != MOE_OK:
+        raise MoEError(st, where)
+
+
+def check_shape(s: MoeShape) -> int:
+    return lib().moe_check_shape(ctypes.byref(s))
+
+
+def workspace_size(s: MoeShape) -> int:
+    return lib().moe_workspace_size(ctypes.byref(s))
+
+
+def hostio_workspace_size(s: MoeShape) -> int:
+    return lib().moe_forward_hostio_workspace_size(ctypes.byref(s))
+
+
+def permute_workspace_size(s: MoeShape) -> int:
+    return lib().moe_permute_workspace_size(ctypes.byref(s))
+
+
+def grouped_ffn_workspace_size(s: MoeShape) -> int:
+    return lib().moe_grouped_ffn_workspace_size(ctypes.byref(s))
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A caller-owned workspace buffer (the library itself never allocates)."""
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def route(s, x, w_g, bias, topk_idx, topk_w, stream=None):
+    _check(lib().moe_route(ctypes.byref(s), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(topk_idx), _ptr(topk_w),
+                           _stream(stream)), "moe_route")
+
+
+def permute(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, stream=None):
+    _check(lib().moe_permute(ctypes.byref(s), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(perm),
+                             _ptr(inv_perm), _ptr(x_perm), _ptr(ws), ws.numel() if ws is not None else 0,
+                             _stream(stream)), "moe_permute")
+
+
+def grouped_ffn(s, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, stream=None):
+    _check(lib().moe_grouped_ffn(ctypes.byref(s), _ptr(x_perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
+                                 _ptr(w_down), _ptr(y_perm), _ptr(ws), ws.numel() if ws is not None else 0,
+                                 _stream(stream)), "moe_grouped_ffn")
+
+
+def combine(s, y_perm, inv_perm, topk_w, out, stream=None):
+    _check(lib().moe_combine(ctypes.byref(s), _ptr(y_perm), _ptr(inv_perm), _ptr(topk_w), _ptr(out),
+                             _stream(stream)), "moe_combine")
+
+
+def forward(s, x, w_g, bias, w_gate, w_up, w_down, out, ws, topk_idx=None, topk_w=None, counts=None, stream=None):
+    _check(lib().moe_forward(ctypes.byref(s), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(w_gate), _ptr(w_up),
+                             _ptr(w_down), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(ws),
+                             ws.numel(), _stream(stream)), "moe_forward")
+
+
+def forward_hostio(s, x_host, w_g, bias, w_gate, w_up, w_down, out_host, ws, stream=None):
+    _check(lib().moe_forward_hostio(ctypes.byref(s), _host_ptr(x_host), _ptr(w_g), _ptr(bias), _ptr(w_gate),
+                                    _ptr(w_up), _ptr(w_down), _host_ptr(out_host), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "moe_forward_hostio")
+
+
+def get_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    return lib().moe_get_error(_stream(stream))
+
+
+def selftest_bounded_wait(timeout_ns: int, stream=None):
+    _check(lib().moe_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "moe_selftest_bounded_wait")
+
+
+def version() -> int:
+    return lib().moe_version()

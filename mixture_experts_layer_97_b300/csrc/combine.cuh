@@ -1,0 +1,89 @@
+// combine.cuh -- K4: weighted un-permute back to token order.
+//
+// "MoE显存与计算开销四阶段手算指南" section 2.4 and
+// "MoE混合专家模型计算原理与推理部署实战解析" sections 2.2 and 5.1 step 5:
+//   out[t,:] = sum_{j<k} w[t,j] * y_perm[inv_perm[t*k+j], :]
+// One warp per token; each lane owns 16-byte column chunks, accumulates the k
+// gathered rows in fp32 in j order and writes the row once. No zero-fill and
+// no atomics, so the result is bitwise reproducible.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kCombineThreads = 256;
+
+template <typename T>
+struct Vec8;  // 8 bf16 (16 B) or 4 fp32 (16 B) per chunk
+
+template <>
+struct Vec8<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  __device__ static void load_acc(const void* p, float w, float* acc) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    acc[0] = fmaf(w, bf16_lo(q.x), acc[0]); acc[1] = fmaf(w, bf16_hi(q.x), acc[1]);
+    acc[2] = fmaf(w, bf16_lo(q.y), acc[2]); acc[3] = fmaf(w, bf16_hi(q.y), acc[3]);
+    acc[4] = fmaf(w, bf16_lo(q.z), acc[4]); acc[5] = fmaf(w, bf16_hi(q.z), acc[5]);
+    acc[6] = fmaf(w, bf16_lo(q.w), acc[6]); acc[7] = fmaf(w, bf16_hi(q.w), acc[7]);
+  }
+  __device__ static void store(void* p, const float* acc) {
+    uint4 q;
+    q.x = pack_bf16x2(acc[0], acc[1]); q.y = pack_bf16x2(acc[2], acc[3]);
+    q.z = pack_bf16x2(acc[4], acc[5]); q.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(p) = q;
+  }
+};
+
+template <>
+struct Vec8<float> {
+  static constexpr int kElems = 4;
+  __device__ static void load_acc(const void* p, float w, float* acc) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    acc[0] = fmaf(w, q.x, acc[0]); acc[1] = fmaf(w, q.y, acc[1]);
+    acc[2] = fmaf(w, q.z, acc[2]); acc[3] = fmaf(w, q.w, acc[3]);
+  }
+  __device__ static void store(void* p, const float* acc) {
+    *reinterpret_cast<float4*>(p) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  }
+};
+
+// UNROLL chunks per lane in flight.
+template <typename T, int UNROLL>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __restrict__ y_perm,
+                                                                  const int32_t* __restrict__ inv_perm,
+                                                                  const float* __restrict__ topk_w, int64_t T_tok,
+                                                                  int d, int k, int64_t A, T* __restrict__ out) {
+  constexpr int E = Vec8<T>::kElems;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (kCombineThreads / 32) + warp;
+  if (t >= T_tok) return;
+  const int nchunk = d / E;
+  for (int c0 = 0; c0 < nchunk; c0 += 32 * UNROLL) {
+    float acc[UNROLL][E];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u)
+#pragma unroll
+      for (int i = 0; i < E; ++i) acc[u][i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int64_t row = inv_perm[t * k + j];
+      const float w = topk_w[t * k + j];
+      if (row < 0 || row >= A) {
+        if (lane == 0 && c0 == 0) record_error(MOE_ERR_CORRUPT);
+        continue;
+      }
+      const T* yr = y_perm + row * d;
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        const int c = c0 + lane + 32 * u;
+        if (c < nchunk) Vec8<T>::load_acc(yr + static_cast<int64_t>(c) * E, w, acc[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int c = c0 + lane + 32 * u;
+      if (c < nchunk) Vec8<T>::store(out + t * d + static_cast<int64_t>(c) * E, acc[u]);
+    }
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,463 @@
+// moe_b300.cu -- the C ABI of libmoe_b300.so (declared in include/moe.h).
+//
+// Host side of every entry point: validate arguments before launching,
+// carve the caller's workspace, build TMA tensor maps, pick kernel variants
+// and launch on the caller's stream. No allocation, no synchronisation
+// (except moe_get_error), no CPU fallback.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <type_traits>
+
+#include "combine.cuh"
+#include "common.cuh"
+#include "ffn_simt.cuh"
+#include "ffn_tc.cuh"
+#include "permute.cuh"
+#include "route.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per bounded device wait
+constexpr int kMaxDevices = 64;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t esize(const moe_shape* s) { return s->dtype == MOE_F32 ? 4 : 2; }
+int64_t n_assign(const moe_shape* s) { return s->T * s->k; }
+
+// Bump allocator over the caller's workspace (base == nullptr: size only).
+struct Carve {
+  uint8_t* base;
+  size_t used = 0;
+  explicit Carve(void* p) : base(static_cast<uint8_t*>(p)) {}
+  template <typename T>
+  T* take(size_t bytes) {
+    T* r = base ? reinterpret_cast<T*>(base + used) : nullptr;
+    used += align_up(bytes);
+    return r;
+  }
+};
+
+int64_t perm_chunks(const moe_shape* s) {
+  const int tpc = perm_tokens_per_chunk(s->k);
+  return (s->T + tpc - 1) / tpc;
+}
+
+size_t permute_ws(const moe_shape* s) { return align_up(sizeof(int32_t) * perm_chunks(s) * s->N); }
+size_t ffn_ws(const moe_shape* s) { return align_up(esize(s) * static_cast<size_t>(n_assign(s)) * s->d_ff); }
+
+struct FwdBufs {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  void* x_perm;
+  void* y_perm;
+  void* perm_ws;
+  void* ffn_ws;
+  void* x_dev;     // hostio only
+  void* out_dev;   // hostio only
+  size_t total;
+};
+
+FwdBufs carve_forward(const moe_shape* s, void* ws, bool hostio) {
+  Carve c(ws);
+  FwdBufs b{};
+  const size_t A = static_cast<size_t>(n_assign(s));
+  const size_t es = esize(s);
+  b.topk_idx = c.take<int32_t>(sizeof(int32_t) * A);
+  b.topk_w = c.take<float>(sizeof(float) * A);
+  b.counts = c.take<int32_t>(sizeof(int32_t) * s->N);
+  b.offsets = c.take<int32_t>(sizeof(int32_t) * (s->N + 1));
+  b.perm = c.take<int32_t>(sizeof(int32_t) * A);
+  b.inv_perm = c.take<int32_t>(sizeof(int32_t) * A);
+  b.x_perm = c.take<uint8_t>(es * A * s->d);
+  b.y_perm = c.take<uint8_t>(es * A * s->d);
+  b.perm_ws = c.take<uint8_t>(permute_ws(s));
+  b.ffn_ws = c.take<uint8_t>(ffn_ws(s));
+  if (hostio) {
+    b.x_dev = c.take<uint8_t>(es * static_cast<size_t>(s->T) * s->d);
+    b.out_dev = c.take<uint8_t>(es * static_cast<size_t>(s->T) * s->d);
+  }
+  b.total = c.used;
+  return b;
+}
+
+moe_status shape_status(const moe_shape* s) {
+  if (s == nullptr) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->d < 1 || s->N < 1 || s->k < 1 || s->d_ff < 1 || s->k > s->N) return MOE_ERR_INVALID_ARG;
+  if (s->act != MOE_SWIGLU && s->act != MOE_GELU_TANH) return MOE_ERR_INVALID_ARG;
+  if (s->dtype != MOE_F32 && s->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (s->N > 256) return MOE_ERR_UNSUPPORTED;
+  if (s->T * static_cast<int64_t>(s->k) >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  const int64_t big = static_cast<int64_t>(s->N) * (s->d > s->d_ff ? s->d : s->d_ff);
+  if (big >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if (s->dtype == MOE_BF16) {
+    if (s->d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (s->d_ff % (s->act == MOE_SWIGLU ? 64 : 128) != 0) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (s->d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+    if (s->d_ff > 65535 * 64 || s->d > 65535 * 64) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+bool ptr_ok(const void* p, bool needed) { return needed ? (p != nullptr && aligned16(p)) : (p == nullptr || aligned16(p)); }
+
+int num_sms() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+moe_status launched() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ---------------------------------------------------------------- route
+template <int EPT, typename TX>
+moe_status launch_route_ept(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx,
+                            float* w, cudaStream_t st) {
+  const size_t smem = route_smem_bytes<EPT>();
+  auto kern = route_kernel<EPT, TX>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int64_t grid = (s->T + kRouteTokens - 1) / kRouteTokens;
+  kern<<<static_cast<unsigned>(grid), kRouteThreads, smem, st>>>(x, wg, bias, static_cast<int>(s->T), s->d, s->N,
+                                                                  s->k, idx, w);
+  return launched();
+}
+
+template <typename TX>
+moe_status launch_route(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx, float* w,
+                        cudaStream_t st) {
+  if (s->T == 0) return MOE_OK;
+  if (s->N <= 16) return launch_route_ept<1, TX>(s, x, wg, bias, idx, w, st);
+  if (s->N <= 32) return launch_route_ept<2, TX>(s, x, wg, bias, idx, w, st);
+  if (s->N <= 64) return launch_route_ept<4, TX>(s, x, wg, bias, idx, w, st);
+  if (s->N <= 128) return launch_route_ept<8, TX>(s, x, wg, bias, idx, w, st);
+  return launch_route_ept<16, TX>(s, x, wg, bias, idx, w, st);
+}
+
+moe_status route_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, int32_t* idx, float* w,
+                      cudaStream_t st) {
+  if (s->dtype == MOE_BF16)
+    return launch_route<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(x), wg, bias, idx, w, st);
+  return launch_route<float>(s, static_cast<const float*>(x), wg, bias, idx, w, st);
+}
+
+// ---------------------------------------------------------------- permute
+moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, int32_t* counts, int32_t* offsets,
+                        int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, cudaStream_t st) {
+  const int64_t C = perm_chunks(s);
+  int32_t* hist = static_cast<int32_t*>(ws);
+  if (C > 0) {
+    permute_hist_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, s->T, s->N, s->k, hist);
+    if (launched() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  permute_scan_kernel<<<1, 256, 0, st>>>(hist, static_cast<int>(C), s->N, counts, offsets);
+  if (launched() != MOE_OK) return MOE_ERR_CUDA;
+  if (C > 0) {
+    permute_scatter_kernel<16><<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(
+        idx, hist, x, s->T, s->N, s->k, static_cast<int64_t>(s->d) * esize(s), perm, inv_perm, x_perm);
+    if (launched() != MOE_OK) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 matrix [rows, cols] row-major; box = box_rows x 64 columns, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One grouped GEMM on the tensor cores: out[rows, Nout-slices] for every expert.
+template <int BN, int EPI>
+moe_status launch_tc(const moe_shape* s, const void* a, int K, const void* b0, const void* b1, int Nout,
+                     const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  using Cfg = TcCfg<BN>;
+  constexpr int HB = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
+  const int64_t A = n_assign(s);
+  CUtensorMap ma, mb0, mb1;
+  if (!make_map(&ma, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kTcBM)) return MOE_ERR_CUDA;
+  const uint64_t brows = static_cast<uint64_t>(s->N) * Nout;
+  if (!make_map(&mb0, b0, brows, static_cast<uint64_t>(K), HB)) return MOE_ERR_CUDA;
+  if (EPI == EPI_SWIGLU) {
+    if (!make_map(&mb1, b1, brows, static_cast<uint64_t>(K), HB)) return MOE_ERR_CUDA;
+  } else {
+    mb1 = mb0;
+  }
+  auto kern = grouped_gemm_tc_kernel<BN, EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmemBytes)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int64_t n_tiles = Nout / HB;
+  const int64_t upper = ((A + kTcBM - 1) / kTcBM + s->N) * n_tiles;
+  const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
+  kern<<<grid, kTcThreads, Cfg::kSmemBytes, st>>>(ma, mb0, mb1, offsets, s->N, static_cast<int>(A), K, Nout,
+                                                  static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs);
+  return launched();
+}
+
+template <int EPI>
+moe_status launch_simt(const moe_shape* s, const void* a, int K, const void* b0, const void* b1, int Nout,
+                       const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  const int64_t A = n_assign(s);
+  dim3 grid(static_cast<unsigned>((A + kSimtBM - 1) / kSimtBM + s->N),
+            static_cast<unsigned>((Nout + kSimtBN - 1) / kSimtBN));
+  grouped_gemm_simt_kernel<EPI><<<grid, 256, 0, st>>>(static_cast<const float*>(a), offsets, s->N,
+                                                      static_cast<int>(A), static_cast<const float*>(b0),
+                                                      static_cast<const float*>(b1), K, Nout,
+                                                      static_cast<float*>(out), ldo);
+  return launched();
+}
+
+moe_status ffn_impl(const moe_shape* s, const void* x_perm, const int32_t* offsets, const void* w_gate,
+                    const void* w_up, const void* w_down, void* y_perm, void* ws, cudaStream_t st) {
+  if (n_assign(s) == 0) return MOE_OK;
+  const int d = s->d, F = s->d_ff;
+  void* h = ws;
+  moe_status r;
+  if (s->dtype == MOE_BF16) {
+    if (s->act == MOE_SWIGLU)
+      r = (F % 128 == 0) ? launch_tc<256, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
+                         : launch_tc<128, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st);
+    else
+      r = (F % 256 == 0) ? launch_tc<256, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st)
+                         : launch_tc<128, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
+    if (r != MOE_OK) return r;
+    return (d % 256 == 0) ? launch_tc<256, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st)
+                          : launch_tc<128, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
+  }
+  r = (s->act == MOE_SWIGLU) ? launch_simt<EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
+                             : launch_simt<EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
+  if (r != MOE_OK) return r;
+  return launch_simt<EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
+}
+
+// ---------------------------------------------------------------- combine
+moe_status combine_impl(const moe_shape* s, const void* y_perm, const int32_t* inv_perm, const float* topk_w,
+                        void* out, cudaStream_t st) {
+  if (s->T == 0) return MOE_OK;
+  const int64_t grid = (s->T + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
+  if (s->dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16, 4><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
+        static_cast<__nv_bfloat16*>(out));
+  else
+    combine_kernel<float, 4><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
+        static_cast<const float*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
+        static_cast<float*>(out));
+  return launched();
+}
+
+moe_status forward_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, const void* w_gate,
+                        const void* w_up, const void* w_down, void* out, int32_t* topk_idx, float* topk_w,
+                        int32_t* counts, const FwdBufs& b, cudaStream_t st) {
+  int32_t* idx = topk_idx ? topk_idx : b.topk_idx;
+  float* w = topk_w ? topk_w : b.topk_w;
+  int32_t* cnt = counts ? counts : b.counts;
+  moe_status r = route_impl(s, x, wg, bias, idx, w, st);
+  if (r != MOE_OK) return r;
+  r = permute_impl(s, idx, x, cnt, b.offsets, b.perm, b.inv_perm, b.x_perm, b.perm_ws, st);
+  if (r != MOE_OK) return r;
+  r = ffn_impl(s, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st);
+  if (r != MOE_OK) return r;
+  return combine_impl(s, b.y_perm, b.inv_perm, w, out, st);
+}
+
+bool weights_ok(const moe_shape* s, const void* w_gate, const void* w_up, const void* w_down) {
+  if (!ptr_ok(w_gate, true) || !ptr_ok(w_down, true)) return false;
+  if (s->act == MOE_SWIGLU) return ptr_ok(w_up, true);
+  return w_up == nullptr;
+}
+
+__global__ void bounded_wait_selftest_kernel(unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(smem_addr(&bar), 0u, &abort_flag, timeout_ns);   // nothing arrives
+  __syncthreads();
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_check_shape(const moe_shape* s) { return shape_status(s); }
+
+size_t moe_permute_workspace_size(const moe_shape* s) { return shape_status(s) == MOE_OK ? permute_ws(s) : 0; }
+
+size_t moe_grouped_ffn_workspace_size(const moe_shape* s) { return shape_status(s) == MOE_OK ? ffn_ws(s) : 0; }
+
+size_t moe_workspace_size(const moe_shape* s) {
+  return shape_status(s) == MOE_OK ? carve_forward(s, nullptr, false).total : 0;
+}
+
+size_t moe_forward_hostio_workspace_size(const moe_shape* s) {
+  return shape_status(s) == MOE_OK ? carve_forward(s, nullptr, true).total : 0;
+}
+
+moe_status moe_route(const moe_shape* s, const void* x, const float* w_g, const float* bias, int32_t* topk_idx,
+                     float* topk_w, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(x, any) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) || !ptr_ok(topk_idx, any) ||
+      !ptr_ok(topk_w, any))
+    return MOE_ERR_INVALID_ARG;
+  return route_impl(s, x, w_g, bias, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const void* x, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, size_t ws_bytes,
+                       void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(topk_idx, any) || !ptr_ok(x, any) || !ptr_ok(counts, true) || !ptr_ok(offsets, true) ||
+      !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, any) || !ptr_ok(ws, permute_ws(s) > 0))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < permute_ws(s)) return MOE_ERR_WORKSPACE;
+  return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_grouped_ffn(const moe_shape* s, const void* x_perm, const int32_t* offsets, const void* w_gate,
+                           const void* w_up, const void* w_down, void* y_perm, void* ws, size_t ws_bytes,
+                           void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(x_perm, any) || !ptr_ok(offsets, true) || !weights_ok(s, w_gate, w_up, w_down) ||
+      !ptr_ok(y_perm, any) || !ptr_ok(ws, ffn_ws(s) > 0))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ffn_ws(s)) return MOE_ERR_WORKSPACE;
+  return ffn_impl(s, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const moe_shape* s, const void* y_perm, const int32_t* inv_perm, const float* topk_w,
+                       void* out, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(y_perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(topk_w, any) || !ptr_ok(out, any))
+    return MOE_ERR_INVALID_ARG;
+  return combine_impl(s, y_perm, inv_perm, topk_w, out, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward(const moe_shape* s, const void* x, const float* w_g, const float* bias, const void* w_gate,
+                       const void* w_up, const void* w_down, void* out, int32_t* topk_idx, float* topk_w,
+                       int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(x, any) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) || !weights_ok(s, w_gate, w_up, w_down) ||
+      !ptr_ok(out, any) || !ptr_ok(topk_idx, false) || !ptr_ok(topk_w, false) || !ptr_ok(counts, false) ||
+      !ptr_ok(ws, true))
+    return MOE_ERR_INVALID_ARG;
+  const FwdBufs b = carve_forward(s, ws, false);
+  if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  return forward_impl(s, x, w_g, bias, w_gate, w_up, w_down, out, topk_idx, topk_w, counts, b,
+                      static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_hostio(const moe_shape* s, const void* x_host, const float* w_g, const float* bias,
+                              const void* w_gate, const void* w_up, const void* w_down, void* out_host, void* ws,
+                              size_t ws_bytes, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if ((any && (x_host == nullptr || out_host == nullptr)) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) ||
+      !weights_ok(s, w_gate, w_up, w_down) || !ptr_ok(ws, true))
+    return MOE_ERR_INVALID_ARG;
+  const FwdBufs b = carve_forward(s, ws, true);
+  if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const size_t bytes = esize(s) * static_cast<size_t>(s->T) * s->d;
+  if (any && cudaMemcpyAsync(b.x_dev, x_host, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess) return MOE_ERR_CUDA;
+  st = forward_impl(s, b.x_dev, w_g, bias, w_gate, w_up, w_down, b.out_dev, nullptr, nullptr, nullptr, b, cs);
+  if (st != MOE_OK) return st;
+  if (any && cudaMemcpyAsync(out_host, b.out_dev, bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_get_error(void* stream) {
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int* word = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&word), g_error_word) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof(int), cudaMemcpyDeviceToHost, cs) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(word, 0, sizeof(int), cs) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(v);
+}
+
+moe_status moe_selftest_bounded_wait(int64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1000000) timeout_ns = 1000000;
+  if (timeout_ns > 2000000000) timeout_ns = 2000000000;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<unsigned long long>(timeout_ns));
+  return launched();
+}
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_CORRUPT: return "corrupt routing data";
+  }
+  return "unknown status";
+}
+
+int moe_version(void) { return 100; }
+
+}  // extern "C"

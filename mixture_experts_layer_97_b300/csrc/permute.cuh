@@ -1,0 +1,180 @@
+// permute.cuh -- K2: group the T*k token-expert assignments by expert.
+//
+// "MoE显存与计算开销四阶段手算指南" section 2.3 and
+// "MoE混合专家模型计算原理与推理部署实战解析" section 5.1 steps 2-3:
+// count per expert, exclusive prefix sum into offsets, then move every
+// assignment's input row into one contiguous buffer ordered by expert.
+//
+// A deterministic stable counting sort by flat index f = t*k + j, in three
+// launches over chunks of whole tokens (at most 2048 assignments each):
+//   hist    per-chunk expert histogram (shared-memory integer atomics: the
+//           counts do not depend on their order)
+//   scan    one CTA: counts, offsets, and the first row of every
+//           (chunk, expert) pair
+//   scatter per chunk: stable ranks from warp __match_any_sync + popc in
+//           flat order, perm / inv_perm, then one warp per token reads the x
+//           row once with 128-bit loads and writes it to its k rows.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kPermThreads = 256;
+constexpr int kPermMaxChunk = 2048;   // assignments per chunk
+constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kPermSub = kPermMaxChunk / kPermWarps;  // assignments per warp
+
+__host__ __device__ inline int perm_tokens_per_chunk(int k) {
+  const int t = kPermMaxChunk / k;
+  return t < 1 ? 1 : t;
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_t* __restrict__ topk_idx, int64_t T,
+                                                                    int N, int k, int32_t* __restrict__ hist) {
+  __shared__ int h[256];
+  const int tpc = perm_tokens_per_chunk(k);
+  const int64_t c = blockIdx.x;
+  const int64_t f0 = c * tpc * k;
+  const int64_t f1 = min(T, (c + 1) * static_cast<int64_t>(tpc)) * k;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) h[n] = 0;
+  __syncthreads();
+  for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+    const int e = topk_idx[f];
+    if (e < 0 || e >= N) {
+      record_error(MOE_ERR_CORRUPT);
+      continue;
+    }
+    atomicAdd(&h[e], 1);
+  }
+  __syncthreads();
+  for (int n = threadIdx.x; n < N; n += blockDim.x) hist[c * N + n] = h[n];
+}
+
+// Single CTA of 256 threads; thread n owns expert n.
+__global__ void __launch_bounds__(256) permute_scan_kernel(int32_t* __restrict__ hist, int n_chunks, int N,
+                                                           int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets) {
+  __shared__ int tot[256];
+  __shared__ int warp_sums[8];
+  const int n = threadIdx.x;
+  int run = 0;
+  if (n < N) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const int v = hist[static_cast<int64_t>(c) * N + n];
+      hist[static_cast<int64_t>(c) * N + n] = run;   // chunk-local base, before the expert offset
+      run += v;
+    }
+  }
+  // exclusive scan of run over experts
+  const int lane = n & 31, w = n >> 5;
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int i = 0; i < w; ++i) wbase += warp_sums[i];
+  const int excl = wbase + incl - run;
+  tot[n] = excl;
+  if (n < N) {
+    counts[n] = run;
+    offsets[n] = excl;
+  }
+  if (n == 255) offsets[N] = wbase + incl;   // total of valid assignments (T*k unless corrupt)
+  __syncthreads();
+  if (n < N) {
+    for (int c = 0; c < n_chunks; ++c) hist[static_cast<int64_t>(c) * N + n] += tot[n];
+  }
+}
+
+template <int VEC_BYTES>
+__global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ base, const void* __restrict__ x, int64_t T,
+    int N, int k, int64_t row_bytes, int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
+    void* __restrict__ x_perm) {
+  __shared__ int wh[kPermWarps][256];
+  __shared__ int rows_s[kPermMaxChunk];
+  const int tpc = perm_tokens_per_chunk(k);
+  const int64_t c = blockIdx.x;
+  const int64_t tok0 = c * tpc;
+  const int ntok = static_cast<int>(min(T, tok0 + static_cast<int64_t>(tpc)) - tok0);
+  const int nf = ntok * k;
+  const int64_t f0 = tok0 * k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+
+  for (int i = threadIdx.x; i < kPermWarps * 256; i += blockDim.x) (&wh[0][0])[i] = 0;
+  __syncthreads();
+
+  const int s0 = warp * kPermSub;
+  const int s1 = min(nf, s0 + kPermSub);
+  // pass 1: per-warp histogram over the warp's contiguous sub-range
+  for (int g = s0; g < s1; g += 32) {
+    const int fl = g + lane;
+    int e = (fl < s1) ? topk_idx[f0 + fl] : -1;
+    if (e >= N) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // pass 2: per-expert prefix over warps, starting at the chunk's base row
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    int run = base[c * N + n];
+#pragma unroll
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int v = wh[w][n];
+      wh[w][n] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // pass 3: stable ranks in flat order
+  for (int g = s0; g < s1; g += 32) {
+    const int fl = g + lane;
+    int e = (fl < s1) ? topk_idx[f0 + fl] : -1;
+    if (e >= N) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int row = -1;
+    if (e >= 0) row = wh[warp][e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
+    __syncwarp();
+    if (fl < s1) {
+      rows_s[fl] = row;
+      inv_perm[f0 + fl] = row;
+      if (row >= 0) perm[row] = static_cast<int32_t>((f0 + fl) / k);
+    }
+  }
+  __syncthreads();
+  // row copies: one warp per token, read once, write to its k rows
+  typedef typename std::conditional<VEC_BYTES == 16, uint4, uint32_t>::type V;
+  const int64_t nv = row_bytes / VEC_BYTES;
+  const V* xs = reinterpret_cast<const V*>(x);
+  V* xp = reinterpret_cast<V*>(x_perm);
+  for (int tl = warp; tl < ntok; tl += kPermWarps) {
+    const int64_t t = tok0 + tl;
+    for (int64_t v0 = 0; v0 < nv; v0 += 32 * 4) {
+      V val[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t v = v0 + lane + 32 * u;
+        if (v < nv) val[u] = xs[t * nv + v];
+      }
+      for (int j = 0; j < k; ++j) {
+        const int row = rows_s[tl * k + j];
+        if (row < 0) continue;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t v = v0 + lane + 32 * u;
+          if (v < nv) xp[static_cast<int64_t>(row) * nv + v] = val[u];
+        }
+      }
+    }
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,406 @@
+"""Benchmark of the MoE layer forward (route -> permute -> grouped FFN -> combine).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). A step is one forward of the whole layer over
+one batch of seeded synthetic tokens with the workload's shapes, through the
+library's C ABI. Under torchrun every rank runs an independent replica of the
+layer on its own tokens (the tokens of a batch are independent, so the work
+shards by batch with no collective); value = tokens of all ranks / max time.
+
+Default workload: the pages' worked example (4 x 2048 tokens, d 4096, 64
+experts, 4096 -> 16384 -> 4096 tanh-GELU experts, top-2, bf16, fp32 gate).
+--impl reference times the CPU oracle instead, on a bounded sample of the
+same workload, on the host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as S  # noqa: E402
+from mixture_experts_layer_97_b300 import accounting as acc  # noqa: E402
+
+DEFAULT_WORKLOAD = "worked-example-n64-f16384-gelu"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p["bf16_tflops_sustained"], src="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    cs = os.path.join(ROOT, "mixture_experts_layer_97_b300", "csrc")
+    for name in sorted(os.listdir(cs)):
+        with open(os.path.join(cs, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the grouped GEMM from a committed ncu capture,
+    valid only while the kernel sources are unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("bytes_per_call")
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [c.strip() for c in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle sample
+def cpu_sample_plan(w: S.Workload, target_rows: int):
+    """A bounded sample of the workload for the CPU oracle: tokens whose k
+    experts all lie in a small expert subset (so only that subset's weights are
+    held on the host), in token order. Routing is the oracle's own."""
+    import oracle
+    x = S.x_all(w)
+    r = oracle.route(x, S.gate_weight(w), w.k, bias=S.gate_bias(w))
+    idx = r["topk_idx"]
+    for n_sub in (8, 16, 24, 32, 48, w.N):
+        sub = np.arange(min(n_sub, w.N))
+        ok = np.all(np.isin(idx, sub), axis=1)
+        toks = np.where(ok)[0]
+        if toks.size * w.k >= target_rows or n_sub >= w.N:
+            toks = toks[:max(1, target_rows // w.k)]
+            used = np.unique(idx[toks])
+            return toks, used
+    raise AssertionError
+
+
+def run_oracle_sample(w: S.Workload, tokens, weights: dict):
+    """One oracle forward of the sampled tokens: route, every selected
+    expert's FFN on its rows, combine. Returns wall seconds."""
+    import oracle
+    x = S.x_all(w)[tokens]
+    wg, b = S.gate_weight(w), S.gate_bias(w)
+    t0 = time.perf_counter()
+    r = oracle.route(x, wg, w.k, bias=b)
+    idx = r["topk_idx"]
+    y = np.zeros((len(tokens) * w.k, w.d))
+    for e in np.unique(idx):
+        q, j = np.nonzero(idx == e)
+        a, bb, c = weights[int(e)]
+        y[q * w.k + j] = oracle.expert_rows(x[q], a, bb, c, w.act)
+    oracle.combine(y, np.arange(len(tokens) * w.k, dtype=np.int32), r["topk_w"])
+    return time.perf_counter() - t0
+
+
+def reference_arm(args, w):
+    """--impl reference: the CPU oracle timed as it stands on a bounded sample."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step_rows = {"worked-example-n64-f16384-gelu": 32, "prefill-n8-f14336": 32,
+                     "zipf-skew-n128-k8": 256, "decode-t32-n64-k8": 256}.get(w.name, 64)
+    tokens, used = cpu_sample_plan(w, per_step_rows)
+    weights = dict(S.iter_expert_weights(w, experts=[int(e) for e in used]))
+    for _ in range(args.warmup):
+        run_oracle_sample(w, tokens, weights)
+    times = [run_oracle_sample(w, tokens, weights) for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    value = len(tokens) / sec
+    sample = (f"{len(tokens)} tokens of {w.name} (route + {len(tokens) * w.k} expert rows + combine) "
+              f"whose experts lie in a {len(used)}-expert subset, same sample every step")
+    line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,
+                       "sample_tokens_per_step": int(len(tokens))},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w0 = S.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w0)
+
+    import torch
+    from mixture_experts_layer_97_b300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    # replicas: same layer shapes, each rank its own seeded tokens and weights
+    w = w0.scaled(seed=w0.seed + 1000 * rank) if rank else w0
+
+    # cpu sample plan first (host only), so its experts can be kept while uploading
+    do_cpu = rank == 0 and not args.no_cpu_baseline
+    if do_cpu:
+        cpu_rows = {"worked-example-n64-f16384-gelu": 384, "prefill-n8-f14336": 128,
+                    "zipf-skew-n128-k8": 4096, "decode-t32-n64-k8": 256}.get(w.name, 256)
+        cpu_tokens, cpu_used = cpu_sample_plan(w, cpu_rows)
+        keep = set(int(e) for e in cpu_used)
+    else:
+        keep = set()
+
+    td = B.TORCH_DTYPE[w.dtype]
+    dev = lambda a: (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+                     else torch.from_numpy(a)).cuda()
+    x_h = S.x_all(w)
+    x = dev(x_h)
+    wg = dev(S.gate_weight(w))
+    b_h = S.gate_bias(w)
+    bias = dev(b_h) if b_h is not None else None
+    WG = torch.empty((w.N, w.F, w.d), dtype=td, device="cuda")
+    WU = torch.empty((w.N, w.F, w.d), dtype=td, device="cuda") if w.act == "swiglu" else None
+    WD = torch.empty((w.N, w.d, w.F), dtype=td, device="cuda")
+    kept = {}
+    for e, (a, b_, c) in S.iter_expert_weights(w):
+        WG[e].copy_(dev(a))
+        if WU is not None:
+            WU[e].copy_(dev(b_))
+        WD[e].copy_(dev(c))
+        if e in keep:
+            kept[e] = (a, b_, c)
+    torch.cuda.synchronize()
+
+    s = B.shape(w.T, w.d, w.N, w.k, w.F, w.act, w.dtype)
+    A = w.A
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    tw = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    counts = torch.empty(w.N, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(w.N + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(A, dtype=torch.int32, device="cuda")
+    inv = torch.empty(A, dtype=torch.int32, device="cuda")
+    xp = torch.empty((A, w.d), dtype=td, device="cuda")
+    yp = torch.empty((A, w.d), dtype=td, device="cuda")
+    out = torch.empty((w.T, w.d), dtype=td, device="cuda")
+    ws = B.workspace(max(B.permute_workspace_size(s), B.grouped_ffn_workspace_size(s)))
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        B.route(s, x, wg, bias, idx, tw)
+        if ev: ev[1].record(stream)
+        B.permute(s, idx, x, counts, offsets, perm, inv, xp, ws)
+        if ev: ev[2].record(stream)
+        B.grouped_ffn(s, xp, offsets, WG, WU, WD, yp, ws)
+        if ev: ev[3].record(stream)
+        B.combine(s, yp, inv, tw, out)
+        if ev: ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = B.get_error()
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device error during warm-up: {B.status_string(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()                      # L2 flush between timed steps (outside the events)
+            step(evs[i])
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    st = B.get_error()
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device error during timing: {B.status_string(st)}")
+    stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
+    step_ms = float(stage.sum(1).mean())
+    ffn_ms = float(stage[:, 2].mean())
+    if dist:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    # end to end through the public host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory() if w.dtype == "bf16" \
+            else torch.from_numpy(x_h).pin_memory()
+        out_host = torch.empty((w.T, w.d), dtype=td).pin_memory()
+        wsh = B.workspace(B.hostio_workspace_size(s))
+        del ws
+        for _ in range(2):
+            B.forward_hostio(s, x_host, wg, bias, WG, WU, WD, out_host, wsh)
+        torch.cuda.synchronize()
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        if dist:
+            dist.barrier()
+        for i in range(args.steps):
+            flush.zero_()
+            e_ev[i][0].record(stream)
+            B.forward_hostio(s, x_host, wg, bias, WG, WU, WD, out_host, wsh)
+            e_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if B.get_error() != B.MOE_OK:
+            raise RuntimeError("device error during the end-to-end run")
+        e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
+        if dist:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        io = w.T * w.d * w.esize
+        e2e = {"value": world * w.T / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": io,
+               "d2h_bytes_per_step": io, "ms_per_step": e_ms}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    P = peaks()
+    cnt = counts.cpu().numpy()
+    up_f, down_f = acc.up_flops(A, w.d, w.F, w.act), acc.down_flops(A, w.d, w.F)
+    ffn_flops = up_f + down_f
+    wbytes = acc.active_expert_weight_bytes(cnt, w.d, w.F, w.act, w.esize)
+    # prefill-shaped (many rows per active expert): tensor roofline; decode-shaped: the HBM bytes of the
+    # active experts' weights. Both fractions are reported.
+    rows_per_active = A / max(1, int((cnt > 0).sum()))
+    tensor_bound = rows_per_active >= 128
+    traffic = recorded_traffic(w.name)
+    tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
+    gbs = wbytes / (ffn_ms * 1e-3) / 1e9
+    if tensor_bound:
+        roof = {"bound": "tensor", "kernel": "grouped_gemm_tc (up + down launches of moe_grouped_ffn)",
+                "achieved": tflops, "peak": P["bf16"], "unit": "TFLOP/s", "frac": tflops / P["bf16"],
+                "peak_kind": f"bf16 burst, {P['src']}", "frac_of_sustained": tflops / P["bf16_sus"],
+                "frac_hbm_weights": gbs / P["hbm"], "traffic": traffic, "algorithmic_flops_per_call": ffn_flops,
+                "algorithmic_weight_bytes_per_call": wbytes}
+    else:
+        roof = {"bound": "hbm", "kernel": "grouped_gemm_tc (up + down launches of moe_grouped_ffn)",
+                "achieved": gbs, "peak": P["hbm"], "unit": "GB/s", "frac": gbs / P["hbm"],
+                "peak_kind": f"copy bandwidth, {P['src']}", "frac_tensor": tflops / P["bf16"], "traffic": traffic,
+                "algorithmic_bytes_per_call": wbytes}
+    fwd_bytes = acc.decode_forward_bytes(cnt, w.T, w.d, w.N, w.k, w.F, w.act, w.esize)
+    roof["forward_frac_hbm"] = fwd_bytes / (step_ms * 1e-3) / 1e9 / P["hbm"]
+
+    cpu = None
+    if do_cpu:
+        import oracle
+        secs = run_oracle_sample(w, cpu_tokens, kept)
+        cpu = {"value": len(cpu_tokens) / secs, "unit": "tokens/s", "cores": oracle.num_threads(),
+               "kind": "oracle",
+               "sample": (f"{len(cpu_tokens)} tokens (route + {len(cpu_tokens) * w.k} expert rows + combine) "
+                          f"whose experts lie in a {len(cpu_used)}-expert subset; {secs:.1f} s")}
+
+    clocks = clk.summary()
+    line = {
+        "metric": "MoE-layer tokens/s", "value": world * w.T / (step_ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,
+                   "gate": "fp32", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (2 x 126 MB write); expert weights also exceed L2"},
+        "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
+        "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
+        "stage_ms": {"route": float(stage[:, 0].mean()), "permute": float(stage[:, 1].mean()),
+                     "grouped_ffn": ffn_ms, "combine": float(stage[:, 3].mean())},
+        "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()),
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 7 * args.steps,
+        "clocks": clocks,
+        "kernel_source": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

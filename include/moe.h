@@ -144,6 +144,34 @@ moe_status moe_forward_hostio(const moe_shape *s, const void *x_host, const floa
                               const void *w_down, void *out_host, void *ws, size_t ws_bytes,
                               void *stream);
 
+/*
+ * moe_permute without a caller workspace. No passage of the pages has a
+ * counterpart: this exists for callers that cannot hand the library device
+ * scratch memory -- for example a host framework that gives a custom operator
+ * only its input and output tensors and no allocator, or latency-critical code
+ * that must not call cudaMalloc (it can synchronise the device) in the middle
+ * of a forward. Outputs and their meaning are exactly those of moe_permute.
+ *
+ * The per-chunk expert histogram lives in a fixed array inside the library
+ * (MOE_PERMUTE_NOALLOC_SCRATCH_INTS int32 values, 256 KiB, held on every
+ * device that loads the library until the process exits). The shape must
+ * satisfy ceil(T / max(1, 2048 / k)) * N <= MOE_PERMUTE_NOALLOC_SCRATCH_INTS
+ * (for example T up to about 1M tokens at k = 2, N = 64); larger shapes return
+ * MOE_ERR_WORKSPACE and launch nothing. The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *
+ * The first call on a device looks up that device's address of the array
+ * (cudaGetSymbolAddress, with the device current); make that first call
+ * before any stream capture. All calls share the one array and it keeps the
+ * last call's contents (every entry a call reads is written first by the same
+ * call, so nothing needs clearing); calls whose work overlaps on the GPU (two
+ * streams at once) race on it and must be serialised by the caller.
+ */
+#define MOE_PERMUTE_NOALLOC_SCRATCH_INTS 65536
+moe_status moe_permute_noalloc(const moe_shape *s, const int32_t *topk_idx, const void *x,
+                               int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                               void *x_perm, void *stream);
+
 /* Workspace sizes in bytes (0 when the shape is invalid or unsupported). */
 size_t moe_workspace_size(const moe_shape *s);
 size_t moe_forward_hostio_workspace_size(const moe_shape *s);

@@ -38,6 +38,7 @@ SIGNATURES = {
     "moe_route": (I32, [SP, P, P, P, P, P, P]),
     "moe_permute": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_grouped_ffn": (I32, [SP, P, P, P, P, P, P, P, SZ, P]),
+    "moe_permute_noalloc": (I32, [SP, P, P, P, P, P, P, P, P]),
     "moe_combine": (I32, [SP, P, P, P, P, P]),
     "moe_forward": (I32, [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_hostio": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
@@ -147,6 +148,13 @@ def permute(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, stream=
     _check(lib().moe_permute(ctypes.byref(s), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(perm),
                              _ptr(inv_perm), _ptr(x_perm), _ptr(ws), ws.numel() if ws is not None else 0,
                              _stream(stream)), "moe_permute")
+
+
+def permute_noalloc(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, stream=None):
+    """moe_permute with its scratch in the library's fixed device array (no workspace argument)."""
+    _check(lib().moe_permute_noalloc(ctypes.byref(s), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
+                                     _ptr(perm), _ptr(inv_perm), _ptr(x_perm), _stream(stream)),
+           "moe_permute_noalloc")
 
 
 def grouped_ffn(s, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, stream=None):

@@ -426,6 +426,33 @@ moe_status moe_forward_hostio(const moe_shape* s, const void* x_host, const floa
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------- permute without a workspace
+// Chunk-histogram scratch of moe_permute_noalloc. Host code must not pass this
+// name to a kernel (on the host it is only a stand-in for the symbol): the
+// device address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) int32_t g_permute_noalloc_scratch[MOE_PERMUTE_NOALLOC_SCRATCH_INTS];
+
+moe_status moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, const void* x, int32_t* counts,
+                               int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* x_perm, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(topk_idx, any) || !ptr_ok(x, any) || !ptr_ok(counts, true) || !ptr_ok(offsets, true) ||
+      !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, any))
+    return MOE_ERR_INVALID_ARG;
+  if (perm_chunks(s) * s->N > MOE_PERMUTE_NOALLOC_SCRATCH_INTS) return MOE_ERR_WORKSPACE;
+  static void* scratch_addr[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  if (scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    scratch_addr[dev] = p;
+  }
+  return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, scratch_addr[dev],
+                      static_cast<cudaStream_t>(stream));
+}
+
 moe_status moe_get_error(void* stream) {
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   int* word = nullptr;

@@ -3,9 +3,10 @@
 // "MoE显存与计算开销四阶段手算指南" section 2.4 and
 // "MoE混合专家模型计算原理与推理部署实战解析" sections 2.2 and 5.1 step 5:
 //   out[t,:] = sum_{j<k} w[t,j] * y_perm[inv_perm[t*k+j], :]
-// One warp per token; each lane owns 16-byte column chunks, accumulates the k
-// gathered rows in fp32 in j order and writes the row once. No zero-fill and
-// no atomics, so the result is bitwise reproducible.
+// A flat grid of warps over (token, group of 16-byte column chunks): each
+// lane accumulates its chunks of the k gathered rows in fp32 in j order and
+// writes them once. No zero-fill and no atomics, so the result is bitwise
+// reproducible.
 #pragma once
 #include "common.cuh"
 
@@ -47,42 +48,48 @@ struct Vec8<float> {
   }
 };
 
-// UNROLL chunks per lane in flight.
-template <typename T, int UNROLL>
+// Warp w owns token t = w / G and a group of 32*CPT 16-byte chunks of the
+// output row, lane strided (each load instruction covers 512 contiguous
+// bytes). The token's k (row, weight) pairs are loaded once per warp.
+template <int CPT>
+__host__ __device__ inline int combine_groups(int nchunk) { return (nchunk + 32 * CPT - 1) / (32 * CPT); }
+
+template <typename T, int CPT>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __restrict__ y_perm,
                                                                   const int32_t* __restrict__ inv_perm,
                                                                   const float* __restrict__ topk_w, int64_t T_tok,
                                                                   int d, int k, int64_t A, T* __restrict__ out) {
   constexpr int E = Vec8<T>::kElems;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * (kCombineThreads / 32) + warp;
-  if (t >= T_tok) return;
   const int nchunk = d / E;
-  for (int c0 = 0; c0 < nchunk; c0 += 32 * UNROLL) {
-    float acc[UNROLL][E];
+  const int G = combine_groups<CPT>(nchunk);
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * kCombineThreads + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= T_tok * G) return;
+  const int64_t t = gw / G;
+  const int c0 = static_cast<int>(gw % G) * 32 * CPT + lane;
+  float acc[CPT][E];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u)
+  for (int u = 0; u < CPT; ++u)
 #pragma unroll
-      for (int i = 0; i < E; ++i) acc[u][i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int64_t row = inv_perm[t * k + j];
-      const float w = topk_w[t * k + j];
-      if (row < 0 || row >= A) {
-        if (lane == 0 && c0 == 0) record_error(MOE_ERR_CORRUPT);
-        continue;
-      }
-      const T* yr = y_perm + row * d;
-#pragma unroll
-      for (int u = 0; u < UNROLL; ++u) {
-        const int c = c0 + lane + 32 * u;
-        if (c < nchunk) Vec8<T>::load_acc(yr + static_cast<int64_t>(c) * E, w, acc[u]);
-      }
+    for (int e = 0; e < E; ++e) acc[u][e] = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int64_t row = inv_perm[t * k + j];
+    const float w = topk_w[t * k + j];
+    if (row < 0 || row >= A) {
+      if (c0 == 0) record_error(MOE_ERR_CORRUPT);
+      continue;
     }
+    const T* yr = y_perm + row * d;
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const int c = c0 + lane + 32 * u;
-      if (c < nchunk) Vec8<T>::store(out + t * d + static_cast<int64_t>(c) * E, acc[u]);
+    for (int u = 0; u < CPT; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nchunk) Vec8<T>::load_acc(yr + static_cast<int64_t>(c) * E, w, acc[u]);
     }
+  }
+#pragma unroll
+  for (int u = 0; u < CPT; ++u) {
+    const int c = c0 + 32 * u;
+    if (c < nchunk) Vec8<T>::store(out + t * d + static_cast<int64_t>(c) * E, acc[u]);
   }
 }
 

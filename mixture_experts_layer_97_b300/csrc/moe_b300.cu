@@ -128,29 +128,41 @@ int num_sms() {
 moe_status launched() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // ---------------------------------------------------------------- route
-template <int EPT, typename TX>
-moe_status launch_route_ept(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx,
+template <int EG, int EPT, int TPT, typename TX>
+moe_status launch_route_cfg(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx,
                             float* w, cudaStream_t st) {
-  const size_t smem = route_smem_bytes<EPT>();
-  auto kern = route_kernel<EPT, TX>;
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+  using Cfg = RouteCfg<EG, EPT, TPT, TX>;
+  auto kern = route_kernel<EG, EPT, TPT, TX>;
+  if (Cfg::kSmem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmem)) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
-  const int64_t grid = (s->T + kRouteTokens - 1) / kRouteTokens;
-  kern<<<static_cast<unsigned>(grid), kRouteThreads, smem, st>>>(x, wg, bias, static_cast<int>(s->T), s->d, s->N,
-                                                                  s->k, idx, w);
+  const int64_t grid = (s->T + Cfg::TM - 1) / Cfg::TM;
+  kern<<<static_cast<unsigned>(grid), kRouteThreads, Cfg::kSmem, st>>>(x, wg, bias, static_cast<int>(s->T), s->d,
+                                                                        s->N, s->k, idx, w);
   return launched();
+}
+
+// Experts padded to NP = EG * EPT (a power of two >= N); tokens per CTA TM =
+// (256 / EG) * TPT: 64 or 32 with EG = 16, 8 with EG = 32.
+template <int EG, int TPT, typename TX>
+moe_status launch_route_tm(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx,
+                           float* w, cudaStream_t st) {
+  if (EG == 16 && s->N <= 16) return launch_route_cfg<EG, 1, TPT, TX>(s, x, wg, bias, idx, w, st);
+  if (s->N <= 32) return launch_route_cfg<EG, 32 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
+  if (s->N <= 64) return launch_route_cfg<EG, 64 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
+  if (s->N <= 128) return launch_route_cfg<EG, 128 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
+  return launch_route_cfg<EG, 256 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
 }
 
 template <typename TX>
 moe_status launch_route(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx, float* w,
                         cudaStream_t st) {
   if (s->T == 0) return MOE_OK;
-  if (s->N <= 16) return launch_route_ept<1, TX>(s, x, wg, bias, idx, w, st);
-  if (s->N <= 32) return launch_route_ept<2, TX>(s, x, wg, bias, idx, w, st);
-  if (s->N <= 64) return launch_route_ept<4, TX>(s, x, wg, bias, idx, w, st);
-  if (s->N <= 128) return launch_route_ept<8, TX>(s, x, wg, bias, idx, w, st);
-  return launch_route_ept<16, TX>(s, x, wg, bias, idx, w, st);
+  const int64_t sms = num_sms();
+  if ((s->T + 63) / 64 >= sms) return launch_route_tm<16, 4, TX>(s, x, wg, bias, idx, w, st);   // 64 tokens/CTA
+  if ((s->T + 31) / 32 >= sms) return launch_route_tm<16, 2, TX>(s, x, wg, bias, idx, w, st);   // 32 tokens/CTA
+  return launch_route_tm<32, 1, TX>(s, x, wg, bias, idx, w, st);                                 // 8 tokens/CTA
 }
 
 moe_status route_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, int32_t* idx, float* w,
@@ -172,8 +184,13 @@ moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, i
   permute_scan_kernel<<<1, 256, 0, st>>>(hist, static_cast<int>(C), s->N, counts, offsets);
   if (launched() != MOE_OK) return MOE_ERR_CUDA;
   if (C > 0) {
-    permute_scatter_kernel<16><<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(
-        idx, hist, x, s->T, s->N, s->k, static_cast<int64_t>(s->d) * esize(s), perm, inv_perm, x_perm);
+    permute_rank_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, hist, s->T, s->N, s->k, perm,
+                                                                            inv_perm);
+    if (launched() != MOE_OK) return MOE_ERR_CUDA;
+    const int64_t nv = static_cast<int64_t>(s->d) * esize(s) / 16;
+    const int64_t warps = s->T * copy_groups(nv);
+    permute_copy_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(
+        inv_perm, static_cast<const uint4*>(x), s->T, s->k, n_assign(s), nv, static_cast<uint4*>(x_perm));
     if (launched() != MOE_OK) return MOE_ERR_CUDA;
   }
   return MOE_OK;
@@ -278,13 +295,16 @@ moe_status ffn_impl(const moe_shape* s, const void* x_perm, const int32_t* offse
 moe_status combine_impl(const moe_shape* s, const void* y_perm, const int32_t* inv_perm, const float* topk_w,
                         void* out, cudaStream_t st) {
   if (s->T == 0) return MOE_OK;
-  const int64_t grid = (s->T + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
+  constexpr int CPT = 2;
+  const int nchunk = s->d / (s->dtype == MOE_BF16 ? 8 : 4);
+  const int64_t warps = s->T * combine_groups<CPT>(nchunk);
+  const int64_t grid = (warps + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
   if (s->dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16, 4><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
+    combine_kernel<__nv_bfloat16, CPT><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
         static_cast<__nv_bfloat16*>(out));
   else
-    combine_kernel<float, 4><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
+    combine_kernel<float, CPT><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
         static_cast<const float*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
         static_cast<float*>(out));
   return launched();

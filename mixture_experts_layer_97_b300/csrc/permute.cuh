@@ -5,15 +5,18 @@
 // count per expert, exclusive prefix sum into offsets, then move every
 // assignment's input row into one contiguous buffer ordered by expert.
 //
-// A deterministic stable counting sort by flat index f = t*k + j, in three
-// launches over chunks of whole tokens (at most 2048 assignments each):
-//   hist    per-chunk expert histogram (shared-memory integer atomics: the
-//           counts do not depend on their order)
+// A deterministic stable counting sort by flat index f = t*k + j, in four
+// launches:
+//   hist    per chunk of whole tokens (at most 2048 assignments): expert
+//           histogram (shared-memory integer atomics: counts do not depend
+//           on their order)
 //   scan    one CTA: counts, offsets, and the first row of every
 //           (chunk, expert) pair
-//   scatter per chunk: stable ranks from warp __match_any_sync + popc in
-//           flat order, perm / inv_perm, then one warp per token reads the x
-//           row once with 128-bit loads and writes it to its k rows.
+//   rank    per chunk: stable ranks from warp __match_any_sync + popc in flat
+//           order -> perm / inv_perm
+//   copy    flat grid of warps over (token, 2 KB slice of its row): each warp
+//           reads its slice of x once with 128-bit loads and writes it to the
+//           token's k rows, so the copy spreads over every SM.
 #pragma once
 #include "common.cuh"
 
@@ -90,13 +93,11 @@ __global__ void __launch_bounds__(256) permute_scan_kernel(int32_t* __restrict__
   }
 }
 
-template <int VEC_BYTES>
-__global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
-    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ base, const void* __restrict__ x, int64_t T,
-    int N, int k, int64_t row_bytes, int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
-    void* __restrict__ x_perm) {
+__global__ void __launch_bounds__(kPermThreads) permute_rank_kernel(const int32_t* __restrict__ topk_idx,
+                                                                    const int32_t* __restrict__ base, int64_t T,
+                                                                    int N, int k, int32_t* __restrict__ perm,
+                                                                    int32_t* __restrict__ inv_perm) {
   __shared__ int wh[kPermWarps][256];
-  __shared__ int rows_s[kPermMaxChunk];
   const int tpc = perm_tokens_per_chunk(k);
   const int64_t c = blockIdx.x;
   const int64_t tok0 = c * tpc;
@@ -144,36 +145,38 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
     __syncwarp();
     if (fl < s1) {
-      rows_s[fl] = row;
       inv_perm[f0 + fl] = row;
       if (row >= 0) perm[row] = static_cast<int32_t>((f0 + fl) / k);
     }
   }
-  __syncthreads();
-  // row copies: one warp per token, read once, write to its k rows
-  typedef typename std::conditional<VEC_BYTES == 16, uint4, uint32_t>::type V;
-  const int64_t nv = row_bytes / VEC_BYTES;
-  const V* xs = reinterpret_cast<const V*>(x);
-  V* xp = reinterpret_cast<V*>(x_perm);
-  for (int tl = warp; tl < ntok; tl += kPermWarps) {
-    const int64_t t = tok0 + tl;
-    for (int64_t v0 = 0; v0 < nv; v0 += 32 * 4) {
-      V val[4];
+}
+
+// Row copies x[t] -> x_perm[inv_perm[t*k+j]] for j < k. Warp w owns token
+// t = w / G and a group of 32*kCopyUnroll 16-byte chunks of its row, lane
+// strided so every load and store instruction covers 512 contiguous bytes.
+constexpr int kCopyUnroll = 4;
+
+__host__ __device__ inline int64_t copy_groups(int64_t nv) { return (nv + 32 * kCopyUnroll - 1) / (32 * kCopyUnroll); }
+
+__global__ void __launch_bounds__(256) permute_copy_kernel(const int32_t* __restrict__ inv_perm,
+                                                           const uint4* __restrict__ x, int64_t T, int k,
+                                                           int64_t A, int64_t nv, uint4* __restrict__ x_perm) {
+  const int64_t G = copy_groups(nv);
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= T * G) return;
+  const int64_t t = gw / G;
+  const int64_t v0 = (gw % G) * 32 * kCopyUnroll + lane;
+  uint4 val[kCopyUnroll];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t v = v0 + lane + 32 * u;
-        if (v < nv) val[u] = xs[t * nv + v];
-      }
-      for (int j = 0; j < k; ++j) {
-        const int row = rows_s[tl * k + j];
-        if (row < 0) continue;
+  for (int u = 0; u < kCopyUnroll; ++u)
+    if (v0 + 32 * u < nv) val[u] = x[t * nv + v0 + 32 * u];
+  for (int j = 0; j < k; ++j) {
+    const int64_t row = inv_perm[t * k + j];
+    if (row < 0 || row >= A) continue;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int64_t v = v0 + lane + 32 * u;
-          if (v < nv) xp[static_cast<int64_t>(row) * nv + v] = val[u];
-        }
-      }
-    }
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (v0 + 32 * u < nv) x_perm[row * nv + v0 + 32 * u] = val[u];
   }
 }
 

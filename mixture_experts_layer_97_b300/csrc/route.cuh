@@ -9,129 +9,179 @@
 // evaluates w_j = exp(s_j - s_max) / sum_j' exp(s_j' - s_max) over the k
 // selected scores only (identical in exact arithmetic).
 //
-// One CTA owns 64 tokens and all N experts (N padded to NP = 16*EPT). The
-// 64 x NP logit tile is accumulated in registers (4 tokens x EPT experts per
-// thread) from 32-wide K slices of x and W_g staged in shared memory, then
-// written to shared memory where one warp per token runs k rounds of a
-// warp-wide argmax. Logits never reach global memory.
+// Each logit is the sequential FMA chain over i = 0..d-1 in index order (one
+// thread owns it from start to end), then one fp32 bias add: the plainest fp32
+// evaluation, so the top-k decision is reproducible bit for bit.
+//
+// One CTA owns TM tokens and all N experts (padded to NP = EG*EPT). K slices
+// of 32 columns of x (raw dtype) and W_g (fp32) stream through a cp.async ring
+// of STAGES buffers. Thread (ty, tx) accumulates TPT tokens x EPT experts in
+// registers; the TM x NP logit tile then goes to shared memory, where one warp
+// per token runs k rounds of a warp-wide argmax. Logits never reach HBM.
+// TM is picked per launch (64, 32 or 8 tokens) so that small batches still
+// spread over many SMs.
 #pragma once
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kRouteTokens = 64;
 constexpr int kRouteBK = 32;
 constexpr int kRouteThreads = 256;
 
-template <int EPT>
-constexpr size_t route_smem_bytes() {
-  constexpr int NP = 16 * EPT;
-  constexpr size_t tiles = sizeof(float) * (kRouteBK * kRouteTokens + kRouteBK * NP);
-  constexpr size_t logits = sizeof(float) * kRouteTokens * (NP + 1);
-  return tiles > logits ? tiles : logits;
+template <int EG, int EPT, int TPT, typename TX>
+struct RouteCfg {
+  static constexpr int NP = EG * EPT;
+  static constexpr int TG = kRouteThreads / EG;
+  static constexpr int TM = TG * TPT;
+  static constexpr int STAGES = NP >= 128 ? 3 : 4;
+  static constexpr int XROW = kRouteBK * static_cast<int>(sizeof(TX)) + 16;  // bytes per token row (+pad)
+  static constexpr int XBYTES = TM * XROW;                                   // one stage of x
+  static constexpr int WBYTES = kRouteBK * NP * 4;                           // one stage of W_g
+  static constexpr size_t kPipe = static_cast<size_t>(STAGES) * (XBYTES + WBYTES);
+  static constexpr size_t kLogits = sizeof(float) * TM * (NP + 1);
+  static constexpr size_t kSmem = kPipe > kLogits ? kPipe : kLogits;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;   // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <typename TX>
-__device__ __forceinline__ void route_load_x8(const TX* p, float* v);
-
-template <>
-__device__ __forceinline__ void route_load_x8<__nv_bfloat16>(const __nv_bfloat16* p, float* v) {
-  uint4 q = *reinterpret_cast<const uint4*>(p);
+// 8 consecutive K elements of one token, widened to fp32.
+__device__ __forceinline__ void load_x8(const __nv_bfloat16* p, float* v) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
   v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
   v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
 }
-
-template <>
-__device__ __forceinline__ void route_load_x8<float>(const float* p, float* v) {
-  float4 a = *reinterpret_cast<const float4*>(p);
-  float4 b = *reinterpret_cast<const float4*>(p + 4);
+__device__ __forceinline__ void load_x8(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ float to_f32(float v) { return v; }
-
-// EPT: experts per thread (NP = 16*EPT >= N). TX: element type of x.
-template <int EPT, typename TX>
+template <int EG, int EPT, int TPT, typename TX>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restrict__ x, const float* __restrict__ wg,
                                                               const float* __restrict__ bias, int T, int d, int N,
                                                               int k, int32_t* __restrict__ topk_idx,
                                                               float* __restrict__ topk_w) {
-  constexpr int NP = 16 * EPT;
-  constexpr int NPR = NP < 32 ? 32 : NP;  // register slots per token for the argmax
+  using C = RouteCfg<EG, EPT, TPT, TX>;
+  constexpr int NP = C::NP, TM = C::TM, S = C::STAGES;
+  constexpr int NPR = NP < 32 ? 32 : NP;   // register slots per token for the argmax
   constexpr int SLOTS = NPR / 32;
-  extern __shared__ __align__(16) float rsm[];
-  float* xs = rsm;                              // [BK][64] (transposed x tile)
-  float* ws = rsm + kRouteBK * kRouteTokens;    // [BK][NP]
-  float* lg = rsm;                              // [64][NP+1] after the K loop
+  constexpr int XCH = kRouteBK * static_cast<int>(sizeof(TX)) / 16;   // 16-byte chunks per token row slice
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  uint8_t* xs = route_smem;                      // [S][TM][XROW bytes]
+  float* ws = reinterpret_cast<float*>(route_smem + S * C::XBYTES);   // [S][BK][NP]
+  float* lg = reinterpret_cast<float*>(route_smem);                   // [TM][NP+1] after the K loop
 
   const int tid = threadIdx.x;
-  const int tx = tid & 15;   // expert group: experts tx + 16*j
-  const int ty = tid >> 4;   // token group: tokens 4*ty .. 4*ty+3
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRouteTokens;
+  const int tx = tid % EG;   // expert group: experts tx*EPT .. tx*EPT+EPT-1
+  const int ty = tid / EG;   // token group: tokens ty*TPT .. ty*TPT+TPT-1
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TM;
+  const int KB = (d + kRouteBK - 1) / kRouteBK;
+  const bool w_vec = (N % 4) == 0;
 
-  float acc[4][EPT];
+  auto issue = [&](int kb) {
+    const int st = kb % S;
+    const int k0 = kb * kRouteBK;
+    const uint32_t xb = smem_addr(xs + st * C::XBYTES);
+    for (int c = tid; c < TM * XCH; c += kRouteThreads) {
+      const int r = c / XCH, q = c % XCH;
+      const int64_t t = t0 + r;
+      const int kk = k0 + q * (16 / static_cast<int>(sizeof(TX)));
+      const bool ok = (t < T) && (kk < d);
+      const TX* src = ok ? x + t * d + kk : x;
+      cp_async16(xb + r * C::XROW + q * 16, src, ok);
+    }
+    const uint32_t wb = smem_addr(ws + st * kRouteBK * NP);
+    if (w_vec) {
+      for (int c = tid; c < kRouteBK * NP / 4; c += kRouteThreads) {
+        const int kr = c / (NP / 4), n4 = (c % (NP / 4)) * 4;
+        const int gk = k0 + kr;
+        const bool ok = (gk < d) && (n4 < N);
+        const float* src = ok ? wg + static_cast<int64_t>(gk) * N + n4 : wg;
+        cp_async16(wb + (kr * NP + n4) * 4, src, ok);
+      }
+    } else {
+      for (int c = tid; c < kRouteBK * NP; c += kRouteThreads) {
+        const int kr = c / NP, n = c % NP;
+        const int gk = k0 + kr;
+        const bool ok = (gk < d) && (n < N);
+        const float* src = ok ? wg + static_cast<int64_t>(gk) * N + n : wg;
+        cp_async4(wb + c * 4, src, ok);
+      }
+    }
+  };
+
+  float acc[TPT][EPT];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < TPT; ++i)
 #pragma unroll
     for (int j = 0; j < EPT; ++j) acc[i][j] = 0.f;
 
-  // x tile loader mapping: token = tid % 64, 8 consecutive k from kq*8.
-  const int ltok = tid & 63;
-  const int lkq = tid >> 6;  // 0..3
-  const bool vec_ok = (d % 8) == 0;
-
-  for (int kb = 0; kb < d; kb += kRouteBK) {
-    {  // x slice -> xs[k][token]
-      const int64_t t = t0 + ltok;
-      const int kk0 = kb + lkq * 8;
-      float v[8];
-      if (t < T && vec_ok && kk0 + 8 <= d) {
-        route_load_x8<TX>(x + t * d + kk0, v);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = (t < T && kk0 + i < d) ? to_f32(x[t * d + kk0 + i]) : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xs[(lkq * 8 + i) * kRouteTokens + ltok] = v[i];
-    }
-    // W_g slice -> ws[k][n]
-    for (int idx = tid; idx < kRouteBK * NP; idx += kRouteThreads) {
-      const int kk = idx / NP, n = idx % NP;
-      const int gk = kb + kk;
-      ws[idx] = (gk < d && n < N) ? wg[static_cast<int64_t>(gk) * N + n] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kRouteBK; ++kk) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[kk * kRouteTokens + ty * 4]);
-      float wv[EPT];
-#pragma unroll
-      for (int j = 0; j < EPT; ++j) wv[j] = ws[kk * NP + tx + 16 * j];
-#pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        acc[0][j] = fmaf(xv.x, wv[j], acc[0][j]);
-        acc[1][j] = fmaf(xv.y, wv[j], acc[1][j]);
-        acc[2][j] = fmaf(xv.z, wv[j], acc[2][j]);
-        acc[3][j] = fmaf(xv.w, wv[j], acc[3][j]);
-      }
-    }
-    __syncthreads();
+  for (int s = 0; s < S - 1; ++s) {
+    if (s < KB) issue(s);
+    cp_async_commit();
   }
+  for (int kb = 0; kb < KB; ++kb) {
+    cp_async_wait<S - 2>();
+    __syncthreads();
+    if (kb + S - 1 < KB) issue(kb + S - 1);
+    cp_async_commit();
+    const int st = kb % S;
+    const uint8_t* xst = xs + st * C::XBYTES;
+    const float* wst = ws + st * kRouteBK * NP;
+#pragma unroll
+    for (int k8 = 0; k8 < kRouteBK; k8 += 8) {
+      float xv[TPT][8];
+#pragma unroll
+      for (int i = 0; i < TPT; ++i)
+        load_x8(reinterpret_cast<const TX*>(xst + (ty * TPT + i) * C::XROW) + k8, xv[i]);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float wv[EPT];
+        const float* wr = wst + (k8 + u) * NP + tx * EPT;
+        if (EPT % 4 == 0) {
+#pragma unroll
+          for (int j = 0; j < EPT; j += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(wr + j);
+            wv[j] = q.x; wv[j + 1] = q.y; wv[j + 2] = q.z; wv[j + 3] = q.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) wv[j] = wr[j];
+        }
+#pragma unroll
+        for (int i = 0; i < TPT; ++i)
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xv[i][u], wv[j], acc[i][j]);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
 
   // logits (+ bias) -> lg[token][n]; padded experts get -inf
 #pragma unroll
   for (int j = 0; j < EPT; ++j) {
-    const int n = tx + 16 * j;
+    const int n = tx * EPT + j;
     const float b = (bias != nullptr && n < N) ? bias[n] : 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) lg[(ty * 4 + i) * (NP + 1) + n] = (n < N) ? acc[i][j] + b : -INFINITY;
+    for (int i = 0; i < TPT; ++i) lg[(ty * TPT + i) * (NP + 1) + n] = (n < N) ? acc[i][j] + b : -INFINITY;
   }
   __syncthreads();
 
   // top-k: one warp per token, k rounds of warp argmax (ties -> lower id)
   const int warp = tid >> 5, lane = tid & 31;
-  for (int tl = warp; tl < kRouteTokens; tl += kRouteThreads / 32) {
+  for (int tl = warp; tl < TM; tl += kRouteThreads / 32) {
     const int64_t t = t0 + tl;
     if (t >= T) break;
     float v[SLOTS];

@@ -72,6 +72,10 @@ WORKLOADS = {
                                   act="swiglu", dtype="bf16", seed=4),
     "zipf-skew-n128-k8": Workload("zipf-skew-n128-k8", T=16384, d=2048, N=128, k=8, F=768,
                                   act="swiglu", dtype="bf16", seed=5, zipf_s=1.2),
+    # profiling slice: the worked example's per-expert shape (~256 rows per expert,
+    # 4096 -> 16384 -> 4096 GELU) with 8 of its 64 experts, 2.1 GB of weights
+    "worked-example-slice-n8": Workload("worked-example-slice-n8", T=1024, d=4096, N=8, k=2, F=16384,
+                                        act="gelu_tanh", dtype="bf16", seed=6),
 }
 
 

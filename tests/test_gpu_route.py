@@ -36,6 +36,11 @@ CASES = [
     (33, 256, 8, 8, "bf16", False),       # k = N
     (70, 100, 5, 5, "f32", True),         # d not a multiple of the K slice, N < 16
     (40, 36, 256, 255, "f32", False),
+    # large batches take the 64- and 32-token-per-CTA variants
+    (10000, 256, 256, 8, "bf16", True),
+    (12000, 64, 5, 2, "f32", False),       # N % 4 != 0: 4-byte copies of W_g
+    (5000, 128, 17, 3, "bf16", False),
+    (6000, 512, 64, 2, "f32", True),
 ]
 
 

@@ -201,6 +201,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens"],
+                    help="tensor-core tiling of the grouped GEMMs (library default: auto)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w0 = S.WORKLOADS[args.workload]
@@ -214,6 +216,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    B.set_ffn_tiling(args.ffn_tiling)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -385,7 +388,7 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,
-                   "gate": "fp32", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "gate": "fp32", "ffn_tiling": args.ffn_tiling, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write); expert weights also exceed L2"},
         "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
@@ -393,7 +396,7 @@ def main():
                      "grouped_ffn": ffn_ms, "combine": float(stage[:, 3].mean())},
         "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": 8 * args.steps,   # route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),
     }

@@ -172,6 +172,25 @@ moe_status moe_permute_noalloc(const moe_shape *s, const int32_t *topk_idx, cons
                                int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                                void *x_perm, void *stream);
 
+/*
+ * Tiling of the bf16 grouped GEMMs in moe_grouped_ffn / moe_forward (process
+ * wide; results agree within the bf16 tolerance, not bit for bit):
+ *   MOE_TILING_ROWS    128 permuted rows x 256 weight rows per tile (weights
+ *                      are the MMA's N side); an expert's last tile is padded
+ *                      up to 128 rows.
+ *   MOE_TILING_TOKENS  128 weight rows x up to 256 tokens per tile (tokens are
+ *                      the MMA's N side, tiles balanced per expert and rounded
+ *                      to 16 rows): little padding when experts hold few rows.
+ *   MOE_TILING_AUTO    per GEMM: token tiles when T*k >= 64*N and the GEMM's
+ *                      reduction length (d for the first, F for the second)
+ *                      is >= 4096, else row tiles (default).
+ * The pages' grouped GEMM ("MoE显存与计算开销四阶段手算指南" section 4.3)
+ * fixes no tiling; this only chooses how the same product is blocked.
+ */
+typedef enum { MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2 } moe_tiling;
+moe_status moe_set_ffn_tiling(int mode);
+int moe_get_ffn_tiling(void);
+
 /* Workspace sizes in bytes (0 when the shape is invalid or unsupported). */
 size_t moe_workspace_size(const moe_shape *s);
 size_t moe_forward_hostio_workspace_size(const moe_shape *s);

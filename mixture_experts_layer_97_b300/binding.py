@@ -20,6 +20,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_CORRUPT = 4, 5, 6
 MOE_F32, MOE_BF16 = 0, 1
 MOE_SWIGLU, MOE_GELU_TANH = 0, 1
+TILING = {"auto": 0, "rows": 1, "tokens": 2}
 ACT = {"swiglu": MOE_SWIGLU, "gelu_tanh": MOE_GELU_TANH}
 DTYPE = {"f32": MOE_F32, "bf16": MOE_BF16}
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -50,6 +51,8 @@ SIGNATURES = {
     "moe_get_error": (I32, [P]),
     "moe_selftest_bounded_wait": (I32, [I64, P]),
     "moe_status_string": (ctypes.c_char_p, [I32]),
+    "moe_set_ffn_tiling": (I32, [ctypes.c_int]),
+    "moe_get_ffn_tiling": (ctypes.c_int, []),
     "moe_version": (ctypes.c_int, []),
 }
 
@@ -187,6 +190,15 @@ def get_error(stream=None) -> int:
 
 def selftest_bounded_wait(timeout_ns: int, stream=None):
     _check(lib().moe_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "moe_selftest_bounded_wait")
+
+
+def set_ffn_tiling(mode: str):
+    """Choose the tensor-core tiling of the grouped GEMMs: "auto", "rows" or "tokens"."""
+    _check(lib().moe_set_ffn_tiling(TILING[mode]), "moe_set_ffn_tiling")
+
+
+def get_ffn_tiling() -> str:
+    return {v: k for k, v in TILING.items()}[lib().moe_get_ffn_tiling()]
 
 
 def version() -> int:

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <type_traits>
@@ -15,6 +16,7 @@
 #include "common.cuh"
 #include "ffn_simt.cuh"
 #include "ffn_tc.cuh"
+#include "ffn_tc_swap.cuh"
 #include "permute.cuh"
 #include "route.cuh"
 
@@ -25,6 +27,8 @@ namespace {
 constexpr size_t kAlign = 256;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s per bounded device wait
 constexpr int kMaxDevices = 64;
+constexpr int kAutoTokenTileMinRowsPerExpert = 64;  // auto tiling: token tiles from this many rows per expert
+constexpr int kAutoTokenTileMinK = 4096;            // ... and this reduction length
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -255,6 +259,48 @@ moe_status launch_tc(const moe_shape* s, const void* a, int K, const void* b0, c
   return launched();
 }
 
+// The same grouped GEMM with weights as the MMA's M side and the tokens of
+// an expert as its N side (balanced token tiles, multiples of 16).
+template <int EPI>
+moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
+                          const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  constexpr int OF = sw_tile_features<EPI>();
+  const int64_t A = n_assign(s);
+  CUtensorMap mx, mw0, mw1;
+  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox)) return MOE_ERR_CUDA;
+  const uint64_t wrows = static_cast<uint64_t>(s->N) * Nout;
+  if (!make_map(&mw0, w0, wrows, static_cast<uint64_t>(K), kSwFM)) return MOE_ERR_CUDA;
+  if (EPI == EPI_SWIGLU) {
+    if (!make_map(&mw1, w1, wrows, static_cast<uint64_t>(K), kSwFM)) return MOE_ERR_CUDA;
+  } else {
+    mw1 = mw0;
+  }
+  auto kern = grouped_gemm_tc_swap_kernel<EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSwSmemBytes)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int64_t n_ftiles = (Nout + OF - 1) / OF;
+  const int64_t upper = ((A + kSwMaxNT - 1) / kSwMaxNT + s->N) * n_ftiles;
+  const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
+  kern<<<grid, kSwThreads, kSwSmemBytes, st>>>(mw0, mw1, mx, offsets, s->N, static_cast<int>(A), K, Nout,
+                                               static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs);
+  return launched();
+}
+
+// Process-wide choice between the two tensor-core tilings (moe_set_ffn_tiling).
+std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
+
+// K is the reduction length of the GEMM in question (d for the first, F for
+// the second). Token tiles pad less but keep one accumulator pair in TMEM, so
+// their epilogue is not overlapped with the next tile: they pay off when an
+// expert holds enough rows to fill tiles and K is long enough to hide it.
+bool use_token_tiles(const moe_shape* s, int K) {
+  const int mode = g_ffn_tiling.load(std::memory_order_relaxed);
+  if (mode == MOE_TILING_TOKENS) return true;
+  if (mode == MOE_TILING_ROWS) return false;
+  return n_assign(s) >= static_cast<int64_t>(kAutoTokenTileMinRowsPerExpert) * s->N && K >= kAutoTokenTileMinK;
+}
+
 template <int EPI>
 moe_status launch_simt(const moe_shape* s, const void* a, int K, const void* b0, const void* b1, int Nout,
                        const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
@@ -275,13 +321,17 @@ moe_status ffn_impl(const moe_shape* s, const void* x_perm, const int32_t* offse
   void* h = ws;
   moe_status r;
   if (s->dtype == MOE_BF16) {
-    if (s->act == MOE_SWIGLU)
+    if (use_token_tiles(s, d))
+      r = (s->act == MOE_SWIGLU) ? launch_tc_swap<EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
+                                 : launch_tc_swap<EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
+    else if (s->act == MOE_SWIGLU)
       r = (F % 128 == 0) ? launch_tc<256, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
                          : launch_tc<128, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st);
     else
       r = (F % 256 == 0) ? launch_tc<256, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st)
                          : launch_tc<128, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
     if (r != MOE_OK) return r;
+    if (use_token_tiles(s, F)) return launch_tc_swap<EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
     return (d % 256 == 0) ? launch_tc<256, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st)
                           : launch_tc<128, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
   }
@@ -472,6 +522,14 @@ moe_status moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, cons
   return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, scratch_addr[dev],
                       static_cast<cudaStream_t>(stream));
 }
+
+moe_status moe_set_ffn_tiling(int mode) {
+  if (mode != MOE_TILING_AUTO && mode != MOE_TILING_ROWS && mode != MOE_TILING_TOKENS) return MOE_ERR_INVALID_ARG;
+  g_ffn_tiling.store(mode, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+int moe_get_ffn_tiling(void) { return g_ffn_tiling.load(std::memory_order_relaxed); }
 
 moe_status moe_get_error(void* stream) {
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

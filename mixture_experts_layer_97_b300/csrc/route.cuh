@@ -81,9 +81,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
   float* ws = reinterpret_cast<float*>(route_smem + S * C::XBYTES);   // [S][BK][NP]
   float* lg = reinterpret_cast<float*>(route_smem);                   // [TM][NP+1] after the K loop
 
+  // Thread (ty, tx) owns tokens ty*TPT + i and experts V*tx + V*EG*m + c
+  // (m < EPT/V, c < V, V = min(EPT, 4)): its W_g reads are V-wide vectors and
+  // the threads of a warp read consecutive vectors, free of bank conflicts.
+  constexpr int V = EPT < 4 ? EPT : 4;
   const int tid = threadIdx.x;
-  const int tx = tid % EG;   // expert group: experts tx*EPT .. tx*EPT+EPT-1
-  const int ty = tid / EG;   // token group: tokens ty*TPT .. ty*TPT+TPT-1
+  const int tx = tid % EG;
+  const int ty = tid / EG;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TM;
   const int KB = (d + kRouteBK - 1) / kRouteBK;
   const bool w_vec = (N % 4) == 0;
@@ -148,16 +152,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         float wv[EPT];
-        const float* wr = wst + (k8 + u) * NP + tx * EPT;
-        if (EPT % 4 == 0) {
+        const float* wr = wst + (k8 + u) * NP + V * tx;
 #pragma unroll
-          for (int j = 0; j < EPT; j += 4) {
-            const float4 q = *reinterpret_cast<const float4*>(wr + j);
-            wv[j] = q.x; wv[j + 1] = q.y; wv[j + 2] = q.z; wv[j + 3] = q.w;
+        for (int m = 0; m < EPT / V; ++m) {
+          if (V == 4) {
+            const float4 q = *reinterpret_cast<const float4*>(wr + V * EG * m);
+            wv[4 * m] = q.x; wv[4 * m + 1] = q.y; wv[4 * m + 2] = q.z; wv[4 * m + 3] = q.w;
+          } else if (V == 2) {
+            const float2 q = *reinterpret_cast<const float2*>(wr + V * EG * m);
+            wv[2 * m] = q.x; wv[2 * m + 1] = q.y;
+          } else {
+            wv[m] = wr[EG * m];
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < EPT; ++j) wv[j] = wr[j];
         }
 #pragma unroll
         for (int i = 0; i < TPT; ++i)
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
   // logits (+ bias) -> lg[token][n]; padded experts get -inf
 #pragma unroll
   for (int j = 0; j < EPT; ++j) {
-    const int n = tx * EPT + j;
+    const int n = V * tx + V * EG * (j / V) + (j % V);
     const float b = (bias != nullptr && n < N) ? bias[n] : 0.f;
 #pragma unroll
     for (int i = 0; i < TPT; ++i) lg[(ty * TPT + i) * (NP + 1) + n] = (n < N) ? acc[i][j] + b : -INFINITY;

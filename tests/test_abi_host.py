@@ -127,3 +127,12 @@ def test_binding_refuses_cpu_tensors(L):
     x = torch.zeros(4, 128, dtype=torch.bfloat16)
     with pytest.raises(RuntimeError, match="CUDA device"):
         B.route(s, x, x, None, x, x)
+
+
+def test_tiling_policy_setter(L):
+    assert B.get_ffn_tiling() == "auto"
+    for m in ("rows", "tokens", "auto"):
+        B.set_ffn_tiling(m)
+        assert B.get_ffn_tiling() == m
+    assert L.moe_set_ffn_tiling(7) == B.MOE_ERR_INVALID_ARG
+    assert B.get_ffn_tiling() == "auto"

@@ -60,6 +60,15 @@ def check(counts, d, F, act, dtype, seed=0):
 
 
 RAGGED = [0, 1, 127, 128, 129, 300, 0, 5]
+# token-tile edges: multiples of 16 and one past, 256 and one past, several tiles
+RAGGED_TOKENS = [16, 17, 256, 257, 0, 31, 513, 1500]
+
+
+@pytest.fixture(params=["rows", "tokens"])
+def tiling(request):
+    B.set_ffn_tiling(request.param)
+    yield request.param
+    B.set_ffn_tiling("auto")
 
 
 @pytest.mark.parametrize("d,F,act", [
@@ -69,16 +78,17 @@ RAGGED = [0, 1, 127, 128, 129, 300, 0, 5]
     (384, 384, "gelu_tanh"),    # up: 128-wide GELU, down 128-wide
     (1024, 512, "swiglu"),      # 16 K-blocks: the smem ring wraps several times
 ])
-def test_ffn_bf16_ragged(d, F, act):
+def test_ffn_bf16_ragged(d, F, act, tiling):
     check(RAGGED, d, F, act, "bf16", seed=d + F)
+    check(RAGGED_TOKENS, d, F, act, "bf16", seed=d + F + 1)
 
 
-def test_ffn_bf16_more_tiles_than_sms():
+def test_ffn_bf16_more_tiles_than_sms(tiling):
     counts = [700, 513, 64, 1, 900, 0, 333, 1500]      # 35 m-tiles x 8 n-tiles > 148
     check(counts, 512, 1024, "swiglu", "bf16", seed=3)
 
 
-def test_ffn_bf16_single_expert_all_rows():
+def test_ffn_bf16_single_expert_all_rows(tiling):
     check([0, 0, 1000, 0], 256, 256, "gelu_tanh", "bf16", seed=4)
 
 
@@ -87,12 +97,12 @@ def test_ffn_f32(d, F, act):
     check([3, 0, 64, 65, 1, 130], d, F, act, "f32", seed=d)
 
 
-def test_ffn_empty():
+def test_ffn_empty(tiling):
     w, xp, ws, off = make_case([0, 0, 0], 128, 64, "swiglu", "bf16", 0)
     assert run_ffn(w, xp, ws, off).shape == (0, 128)
 
 
-def test_ffn_repeatable_bitwise():
+def test_ffn_repeatable_bitwise(tiling):
     w, xp, ws, off = make_case(RAGGED, 256, 384, "swiglu", "bf16", 9)
     a = run_ffn(w, xp, ws, off)
     b = run_ffn(w, xp, ws, off)
@@ -100,7 +110,7 @@ def test_ffn_repeatable_bitwise():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_ffn_corrupt_offsets_recorded(dtype):
+def test_ffn_corrupt_offsets_recorded(dtype, tiling):
     w, xp, ws, off = make_case([10, 20, 30], 128, 128, "swiglu", dtype, 0)
     bad = off.copy()
     bad[3] = 59                                       # does not add up to A = 60
@@ -111,3 +121,19 @@ def test_ffn_corrupt_offsets_recorded(dtype):
     B.grouped_ffn(s, dev(xp), dev(bad), stack(0), stack(1), stack(2), y, wsb)
     assert B.get_error() == B.MOE_ERR_CORRUPT
     assert float(y.float().abs().max()) == 0.0       # nothing written
+
+
+def test_tilings_agree_within_tolerance():
+    """Both tensor-core tilings compute the same product (only the blocking and
+    the bf16 rounding of h differ): each is within tolerance of the oracle and
+    of each other."""
+    w, xp, ws, off = make_case([200, 0, 300, 45, 1000], 512, 384, "swiglu", "bf16", 12)
+    outs = {}
+    for mode in ("rows", "tokens"):
+        B.set_ffn_tiling(mode)
+        outs[mode] = run_ffn(w, xp, ws, off)
+    B.set_ffn_tiling("auto")
+    ref = oracle_ffn(w, xp, ws, off)
+    for mode, got in outs.items():
+        assert rel_err(got, ref) <= tol("bf16"), mode
+    assert rel_err(outs["rows"], outs["tokens"]) <= tol("bf16")

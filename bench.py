@@ -124,6 +124,28 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ replicas
+def replica_workload(w: S.Workload, rank: int) -> S.Workload:
+    """Rank r runs the same layer shapes on its own seeded tokens and weights
+    (tokens of a batch are independent: the work shards by batch, weak scaling)."""
+    return w.scaled(seed=w.seed + 1000 * rank) if rank else w
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The job's time is the slowest rank's (max over ranks; identity at N=1)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job tokens/s: the tokens of all ranks over the max-over-ranks time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ oracle sample
 def cpu_sample_plan(w: S.Workload, target_rows: int):
     """A bounded sample of the workload for the CPU oracle: tokens whose k
@@ -221,8 +243,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    # replicas: same layer shapes, each rank its own seeded tokens and weights
-    w = w0.scaled(seed=w0.seed + 1000 * rank) if rank else w0
+    w = replica_workload(w0, rank)
 
     # cpu sample plan first (host only), so its experts can be kept while uploading
     do_cpu = rank == 0 and not args.no_cpu_baseline
@@ -305,10 +326,7 @@ def main():
     stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
     step_ms = float(stage.sum(1).mean())
     ffn_ms = float(stage[:, 2].mean())
-    if dist:
-        t = torch.tensor([step_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, dist, "cuda")
 
     # end to end through the public host-buffer entry point
     e2e = None
@@ -334,12 +352,9 @@ def main():
         if B.get_error() != B.MOE_OK:
             raise RuntimeError("device error during the end-to-end run")
         e_ms = float(np.mean([a.elapsed_time(b) for a, b in e_ev]))
-        if dist:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, dist, "cuda")
         io = w.T * w.d * w.esize
-        e2e = {"value": world * w.T / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": io,
+        e2e = {"value": job_throughput(w.T, world, e_ms), "unit": "tokens/s", "h2d_bytes_per_step": io,
                "d2h_bytes_per_step": io, "ms_per_step": e_ms}
 
     if rank != 0:
@@ -384,7 +399,7 @@ def main():
 
     clocks = clk.summary()
     line = {
-        "metric": "MoE-layer tokens/s", "value": world * w.T / (step_ms * 1e-3), "unit": "tokens/s",
+        "metric": "MoE-layer tokens/s", "value": job_throughput(w.T, world, step_ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,

@@ -176,6 +176,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// The same for a tile whose K-major rows are ROW_BYTES long (128, 64 or 32),
+// written by TMA with the matching swizzle (128 B, 64 B or 32 B); 8-row groups
+// are 8 * ROW_BYTES apart and the tile base is aligned to 8 * ROW_BYTES.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t kmajor_swizzled_desc(uint32_t saddr) {
+  static_assert(ROW_BYTES == 128 || ROW_BYTES == 64 || ROW_BYTES == 32, "swizzle width");
+  constexpr uint64_t layout = ROW_BYTES == 128 ? 2 : (ROW_BYTES == 64 ? 4 : 6);
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);            // start address
+  d |= static_cast<uint64_t>(1) << 16;                             // leading byte offset (unused here)
+  d |= static_cast<uint64_t>((8 * ROW_BYTES) >> 4) << 32;          // stride byte offset: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                             // descriptor version
+  d |= layout << 61;                                               // swizzle mode
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B, fp32 D, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                    // D format: f32

@@ -33,18 +33,27 @@ namespace moe {
 constexpr int kSwFM = 128;                 // MMA M: weight rows per MMA
 constexpr int kSwMaxNT = 256;              // MMA N: token rows per tile (max)
 constexpr int kSwBox = 32;                 // token rows per TMA box
-constexpr int kSwWBytes = kSwFM * kTcBK * 2;            // one 128-row weight block per k-block
-constexpr int kSwABytes = 2 * kSwWBytes;                // the pair of weight blocks per stage
-constexpr int kSwBBytes = kSwMaxNT * kTcBK * 2;         // token block per stage
-constexpr int kSwStageBytes = kSwABytes + kSwBBytes;
-constexpr int kSwStages = 3;
 constexpr int kSwEpiWarps = 8;             // two warps per TMEM lane quarter
 constexpr int kSwThreads = 32 * (2 + kSwEpiWarps);   // TMA, MMA, 8 epilogue warps
 constexpr int kSwTmemCols = 2 * kSwMaxNT;               // D0 at column 0, D1 at column 256
 constexpr int kSwXposeBytes = kSwEpiWarps * 32 * 64;    // one 32 x 32 bf16 tile per epilogue warp
-constexpr int kSwNumBars = 2 * kSwStages + 3;
-constexpr size_t kSwSmemBytes = 1024 + static_cast<size_t>(kSwStages) * kSwStageBytes + kSwXposeBytes +
-                                8 * kSwNumBars + 16 + 2 * 257 * sizeof(int) + 16;
+constexpr int kSwRingBudget = 192 * 1024;
+
+// Ring geometry for a K depth of BK elements per stage (BK = 64: 128-byte
+// swizzled rows, 3 stages; BK = 32: 64-byte rows, 6 stages). BK = 64 is the
+// one launched: the 64-byte-swizzle variant measured ~45 % slower.
+template <int BK>
+struct SwCfg {
+  static constexpr int kRowBytes = BK * 2;
+  static constexpr int kWBytes = kSwFM * kRowBytes;              // one 128-row weight block
+  static constexpr int kABytes = 2 * kWBytes;                    // the pair of weight blocks
+  static constexpr int kBBytes = kSwMaxNT * kRowBytes;           // token block
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kSwRingBudget / kStageBytes;
+  static constexpr int kNumBars = 2 * kStages + 3;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + kSwXposeBytes +
+                                       8 * kNumBars + 16 + 2 * 257 * sizeof(int) + 16;
+};
 
 // Output features covered by one tile: SwiGLU 128 (gate/up pair), else 256.
 template <int EPI>
@@ -113,28 +122,29 @@ __device__ __forceinline__ void sw_store_transposed(const uint32_t* v, uint8_t* 
   __syncwarp();
 }
 
-template <int EPI>
+template <int EPI, int BK>
 __global__ void __launch_bounds__(kSwThreads, 1)
     grouped_gemm_tc_swap_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                                 const __grid_constant__ CUtensorMap tmX, const int32_t* __restrict__ offsets, int N,
                                 int rows_total, int K, int Nout, __nv_bfloat16* __restrict__ out, int ldo,
                                 unsigned long long timeout_ns) {
-  constexpr int S = kSwStages;
+  using C = SwCfg<BK>;
+  constexpr int S = C::kStages;
   constexpr int OF = sw_tile_features<EPI>();
   constexpr uint32_t IDESC0 = idesc_bf16_f32(kSwFM, 16) & ~(0x3Fu << 17);   // N field filled per tile
 
   extern __shared__ uint8_t sw_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sw_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_a = smem;                      // S x (W0 block | W1 block)
-  uint8_t* stage_b = smem + S * kSwABytes;      // S x token block
-  uint8_t* xpose = smem + S * kSwStageBytes;
+  uint8_t* stage_b = smem + S * C::kABytes;     // S x token block
+  uint8_t* xpose = smem + S * C::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(xpose + kSwXposeBytes);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + S;
   uint64_t* tfull_bar = bars + 2 * S;
   uint64_t* tempty_bar = tfull_bar + 1;
   uint64_t* drain_bar = tfull_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kSwNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bad_flag = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   if (bad && threadIdx.x == 0 && blockIdx.x == 0) record_error(MOE_ERR_CORRUPT);
   const int n_ftiles = (Nout + OF - 1) / OF;
   const long long total = bad ? 0 : static_cast<long long>(s_pre[N]) * n_ftiles;
-  const int KB = K / kTcBK;
+  const int KB = K / BK;
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
@@ -188,7 +198,7 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const int w0row = t.e * Nout + t.fi * OF;
       const int w1row = (EPI == EPI_SWIGLU) ? w0row : w0row + kSwFM;
       const int nbox = (t.nt + kSwBox - 1) / kSwBox;
-      const uint32_t tx_bytes = kSwABytes + nbox * kSwBox * kTcBK * 2;
+      const uint32_t tx_bytes = C::kABytes + nbox * kSwBox * C::kRowBytes;
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait_bounded(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag, timeout_ns)) {
           ok = false;
@@ -196,12 +206,12 @@ __global__ void __launch_bounds__(kSwThreads, 1)
         }
         const uint32_t fb = smem_addr(&full_bar[s]);
         mbar_arrive_expect_tx(fb, tx_bytes);
-        const uint32_t sa = smem_addr(stage_a + s * kSwABytes);
-        const uint32_t sb = smem_addr(stage_b + s * kSwBBytes);
-        tma_load_2d(sa, &tmW0, fb, kb * kTcBK, w0row);
-        tma_load_2d(sa + kSwWBytes, (EPI == EPI_SWIGLU) ? &tmW1 : &tmW0, fb, kb * kTcBK, w1row);
+        const uint32_t sa = smem_addr(stage_a + s * C::kABytes);
+        const uint32_t sb = smem_addr(stage_b + s * C::kBBytes);
+        tma_load_2d(sa, &tmW0, fb, kb * BK, w0row);
+        tma_load_2d(sa + C::kWBytes, (EPI == EPI_SWIGLU) ? &tmW1 : &tmW0, fb, kb * BK, w1row);
         for (int b = 0; b < nbox; ++b)
-          tma_load_2d(sb + b * kSwBox * kTcBK * 2, &tmX, fb, kb * kTcBK, t.row0 + b * kSwBox);
+          tma_load_2d(sb + b * kSwBox * C::kRowBytes, &tmX, fb, kb * BK, t.row0 + b * kSwBox);
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
       }
@@ -229,11 +239,11 @@ __global__ void __launch_bounds__(kSwThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t a0 = sw128_kmajor_desc(smem_addr(stage_a + s * kSwABytes));
-        const uint64_t a1 = sw128_kmajor_desc(smem_addr(stage_a + s * kSwABytes + kSwWBytes));
-        const uint64_t bd = sw128_kmajor_desc(smem_addr(stage_b + s * kSwBBytes));
+        const uint64_t a0 = kmajor_swizzled_desc<C::kRowBytes>(smem_addr(stage_a + s * C::kABytes));
+        const uint64_t a1 = kmajor_swizzled_desc<C::kRowBytes>(smem_addr(stage_a + s * C::kABytes + C::kWBytes));
+        const uint64_t bd = kmajor_swizzled_desc<C::kRowBytes>(smem_addr(stage_b + s * C::kBBytes));
 #pragma unroll
-        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+        for (int kk = 0; kk < BK / 16; ++kk) {
           const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
           umma_bf16(tmem_base, a0 + 2u * kk, bd + 2u * kk, idesc, acc);
           umma_bf16(tmem_base + kSwMaxNT, a1 + 2u * kk, bd + 2u * kk, idesc, acc);

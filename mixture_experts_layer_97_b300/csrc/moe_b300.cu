@@ -147,26 +147,45 @@ moe_status launch_route_cfg(const moe_shape* s, const TX* x, const float* wg, co
   return launched();
 }
 
-// Experts padded to NP = EG * EPT (a power of two >= N); tokens per CTA TM =
-// (256 / EG) * TPT: 64 or 32 with EG = 16, 8 with EG = 32.
+// Experts padded to NP = EG * EPT, the smallest power of two >= max(N, EG);
+// tokens per CTA TM = (256 / EG) * TPT.
 template <int EG, int TPT, typename TX>
 moe_status launch_route_tm(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx,
                            float* w, cudaStream_t st) {
-  if (EG == 16 && s->N <= 16) return launch_route_cfg<EG, 1, TPT, TX>(s, x, wg, bias, idx, w, st);
-  if (s->N <= 32) return launch_route_cfg<EG, 32 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
-  if (s->N <= 64) return launch_route_cfg<EG, 64 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
-  if (s->N <= 128) return launch_route_cfg<EG, 128 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
-  return launch_route_cfg<EG, 256 / EG, TPT, TX>(s, x, wg, bias, idx, w, st);
+  if (s->N <= EG) return launch_route_cfg<EG, 1, TPT, TX>(s, x, wg, bias, idx, w, st);
+  if constexpr (EG * 2 <= 256) {
+    if (s->N <= EG * 2) return launch_route_cfg<EG, 2, TPT, TX>(s, x, wg, bias, idx, w, st);
+  }
+  if constexpr (EG * 4 <= 256) {
+    if (s->N <= EG * 4) return launch_route_cfg<EG, 4, TPT, TX>(s, x, wg, bias, idx, w, st);
+  }
+  if constexpr (EG * 8 <= 256) {
+    if (s->N <= EG * 8) return launch_route_cfg<EG, 8, TPT, TX>(s, x, wg, bias, idx, w, st);
+  }
+  if constexpr (EG * 16 <= 256) {
+    if (s->N <= EG * 16) return launch_route_cfg<EG, 16, TPT, TX>(s, x, wg, bias, idx, w, st);
+  }
+  return MOE_ERR_UNSUPPORTED;
 }
 
+// Each logit is one thread's sequential chain over d, so parallelism comes
+// from tokens x experts: pick the largest token tile that still gives every
+// SM a CTA, down to 4 tokens per CTA for decode-sized batches.
 template <typename TX>
 moe_status launch_route(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx, float* w,
                         cudaStream_t st) {
   if (s->T == 0) return MOE_OK;
   const int64_t sms = num_sms();
-  if ((s->T + 63) / 64 >= sms) return launch_route_tm<16, 4, TX>(s, x, wg, bias, idx, w, st);   // 64 tokens/CTA
-  if ((s->T + 31) / 32 >= sms) return launch_route_tm<16, 2, TX>(s, x, wg, bias, idx, w, st);   // 32 tokens/CTA
-  return launch_route_tm<32, 1, TX>(s, x, wg, bias, idx, w, st);                                 // 8 tokens/CTA
+  const int64_t T = s->T;
+  if (s->N <= 8) {   // 8 expert lanes: few experts are not padded to 16 or 32
+    if ((T + 127) / 128 >= sms) return launch_route_tm<8, 4, TX>(s, x, wg, bias, idx, w, st);   // 128 tokens/CTA
+    if ((T + 63) / 64 >= sms) return launch_route_tm<8, 2, TX>(s, x, wg, bias, idx, w, st);     // 64 tokens/CTA
+    return launch_route_tm<8, 1, TX>(s, x, wg, bias, idx, w, st);                                // 32 tokens/CTA
+  }
+  if ((T + 63) / 64 >= sms) return launch_route_tm<16, 4, TX>(s, x, wg, bias, idx, w, st);       // 64 tokens/CTA
+  if ((T + 31) / 32 >= sms) return launch_route_tm<16, 2, TX>(s, x, wg, bias, idx, w, st);       // 32 tokens/CTA
+  if ((T + 7) / 8 >= sms / 2) return launch_route_tm<32, 1, TX>(s, x, wg, bias, idx, w, st);     // 8 tokens/CTA
+  return launch_route_tm<64, 1, TX>(s, x, wg, bias, idx, w, st);                                 // 4 tokens/CTA
 }
 
 moe_status route_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, int32_t* idx, float* w,
@@ -218,16 +237,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, cols] row-major; box = box_rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// bf16 matrix [rows, cols] row-major; box = box_rows x box_cols columns with the
+// swizzle whose span is one box row (box_cols * 2 bytes: 128 or 64).
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint32_t box_cols = kTcBK) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), box_rows};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -261,30 +283,37 @@ moe_status launch_tc(const moe_shape* s, const void* a, int K, const void* b0, c
 
 // The same grouped GEMM with weights as the MMA's M side and the tokens of
 // an expert as its N side (balanced token tiles, multiples of 16).
-template <int EPI>
-moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
-                          const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+template <int EPI, int BK>
+moe_status launch_tc_swap_bk(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
+                             const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  using Cfg = SwCfg<BK>;
   constexpr int OF = sw_tile_features<EPI>();
   const int64_t A = n_assign(s);
   CUtensorMap mx, mw0, mw1;
-  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox)) return MOE_ERR_CUDA;
+  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox, BK)) return MOE_ERR_CUDA;
   const uint64_t wrows = static_cast<uint64_t>(s->N) * Nout;
-  if (!make_map(&mw0, w0, wrows, static_cast<uint64_t>(K), kSwFM)) return MOE_ERR_CUDA;
+  if (!make_map(&mw0, w0, wrows, static_cast<uint64_t>(K), kSwFM, BK)) return MOE_ERR_CUDA;
   if (EPI == EPI_SWIGLU) {
-    if (!make_map(&mw1, w1, wrows, static_cast<uint64_t>(K), kSwFM)) return MOE_ERR_CUDA;
+    if (!make_map(&mw1, w1, wrows, static_cast<uint64_t>(K), kSwFM, BK)) return MOE_ERR_CUDA;
   } else {
     mw1 = mw0;
   }
-  auto kern = grouped_gemm_tc_swap_kernel<EPI>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSwSmemBytes)) !=
+  auto kern = grouped_gemm_tc_swap_kernel<EPI, BK>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmemBytes)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   const int64_t n_ftiles = (Nout + OF - 1) / OF;
   const int64_t upper = ((A + kSwMaxNT - 1) / kSwMaxNT + s->N) * n_ftiles;
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
-  kern<<<grid, kSwThreads, kSwSmemBytes, st>>>(mw0, mw1, mx, offsets, s->N, static_cast<int>(A), K, Nout,
-                                               static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs);
+  kern<<<grid, kSwThreads, Cfg::kSmemBytes, st>>>(mw0, mw1, mx, offsets, s->N, static_cast<int>(A), K, Nout,
+                                                  static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs);
   return launched();
+}
+
+template <int EPI>
+moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
+                          const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
 }
 
 // Process-wide choice between the two tensor-core tilings (moe_set_ffn_tiling).

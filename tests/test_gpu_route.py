@@ -36,11 +36,13 @@ CASES = [
     (33, 256, 8, 8, "bf16", False),       # k = N
     (70, 100, 5, 5, "f32", True),         # d not a multiple of the K slice, N < 16
     (40, 36, 256, 255, "f32", False),
-    # large batches take the 64- and 32-token-per-CTA variants
+    # token tile per CTA: 4 (small batches), 8, 32, 64 (and 32/64/128 with <= 8 experts)
     (10000, 256, 256, 8, "bf16", True),
     (12000, 64, 5, 2, "f32", False),       # N % 4 != 0: 4-byte copies of W_g
     (5000, 128, 17, 3, "bf16", False),
     (6000, 512, 64, 2, "f32", True),
+    (1000, 256, 64, 4, "bf16", False),     # 8 tokens per CTA
+    (20000, 128, 8, 2, "bf16", True),      # 8 expert lanes, 128 tokens per CTA
 ]
 
 

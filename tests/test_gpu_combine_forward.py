@@ -152,3 +152,30 @@ def test_forward_full_size(name):
     # the one-call forward gives the same bits as the staged calls
     out1 = run_forward(inp)[0]
     assert torch.equal(out1, r["out"])
+
+
+def test_forward_captured_in_cuda_graph_replays_identically():
+    """The forward only queues work on the caller's stream (no allocation, no
+    host sync), so it can be captured once and replayed; the replay gives the
+    same bits as a direct call, also after the inputs change in place."""
+    w = SMALL[3]
+    inp = Inputs(w)
+    s = inp.shape
+    out = new((w.T, w.d), w.dtype)
+    ws = B.workspace(B.workspace_size(s))
+    B.forward(s, inp.x, inp.wg, inp.bias, inp.w_gate, inp.w_up, inp.w_down, out, ws)   # warm-up, outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            B.forward(s, inp.x, inp.wg, inp.bias, inp.w_gate, inp.w_up, inp.w_down, out, ws)
+    g.replay()
+    torch.cuda.synchronize()
+    direct = run_forward(inp)[0]
+    assert torch.equal(out, direct)
+    inp.x.mul_(-1.0)                                  # new inputs, same buffers
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, run_forward(inp)[0])
+    assert B.get_error() == B.MOE_OK

@@ -57,6 +57,10 @@ def lib():
         L.oracle_route.restype = I
         L.oracle_permute.argtypes = [I64, I, I, P, P, P, P, P]
         L.oracle_permute.restype = I
+        L.oracle_capacity.argtypes = [I64, I, I, ctypes.c_double]
+        L.oracle_capacity.restype = I64
+        L.oracle_permute_capacity.argtypes = [I64, I, I, P, I64, P, P, P, P]
+        L.oracle_permute_capacity.restype = I64
         L.oracle_expert_rows.argtypes = [I64, I, I, I, P, I, P, P, P, I, P, P]
         L.oracle_expert_rows.restype = I
         L.oracle_combine.argtypes = [I64, P, I, I, P, P, P, P]
@@ -129,6 +133,27 @@ def permute(topk_idx, N):
     if rc:
         raise ValueError("oracle_permute: expert index out of range")
     return dict(counts=counts, offsets=offsets, perm=perm, inv_perm=inv)
+
+
+def capacity(T, N, k, capacity_factor) -> int:
+    """Rows an expert may take: ceil(capacity_factor * T * k / N)."""
+    return int(lib().oracle_capacity(T, N, k, float(capacity_factor)))
+
+
+def permute_capacity(topk_idx, N, cap):
+    """Grouping with an expert capacity: kept counts, offsets, perm and
+    inv_perm (-2 for a dropped assignment), and the number dropped."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    counts = np.empty(N, np.int32)
+    offsets = np.empty(N + 1, np.int32)
+    perm = np.full(T * k, -1, np.int32)
+    inv = np.empty(T * k, np.int32)
+    dropped = lib().oracle_permute_capacity(T, N, k, _p(idx), int(cap), _p(counts), _p(offsets), _p(perm), _p(inv))
+    if dropped < 0:
+        raise ValueError("oracle_permute_capacity: expert index out of range")
+    kept = int(offsets[N])
+    return dict(counts=counts, offsets=offsets, perm=perm[:kept], inv_perm=inv, dropped=int(dropped))
 
 
 def expert_rows(x_rows, w_gate, w_up, w_down, act, want_h=False):

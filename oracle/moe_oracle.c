@@ -225,6 +225,58 @@ int oracle_permute(int64_t T, int N, int k, const int32_t *topk_idx,
     return 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * Grouping with an expert capacity: [P3] s4.3. At inference an expert takes
+ * at most `capacity` assignments; the rest are dropped (the token skips that
+ * expert and only the residual path carries it). Readings: capacity counts
+ * assignments, capacity = ceil(capacity_factor * T * k / N) (oracle_capacity);
+ * an expert keeps its assignments in flat order t*k + j, so the earliest
+ * `capacity` are kept; a dropped assignment contributes nothing to the output
+ * and the kept gate weights are not renormalised again.
+ *   counts[n]  kept assignments of expert n = min(demand, capacity)
+ *   offsets    exclusive prefix sum of the kept counts
+ *   perm[row] = t for kept rows; inv_perm[f] = row, or -2 when dropped
+ * Returns the number of dropped assignments, or -1 on a bad index.
+ * ------------------------------------------------------------------------- */
+int64_t oracle_capacity(int64_t T, int N, int k, double capacity_factor)
+{
+    return (int64_t)ceil(capacity_factor * (double)T * (double)k / (double)N);
+}
+
+int64_t oracle_permute_capacity(int64_t T, int N, int k, const int32_t *topk_idx, int64_t capacity,
+                                int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm)
+{
+    const int64_t A = T * k;
+    int64_t *demand = (int64_t *)calloc((size_t)N, sizeof(int64_t));
+    if (!demand) return -1;
+    for (int64_t f = 0; f < A; ++f) {
+        int e = topk_idx[f];
+        if (e < 0 || e >= N) { free(demand); return -1; }
+        demand[e] += 1;
+    }
+    offsets[0] = 0;
+    for (int n = 0; n < N; ++n) {
+        counts[n] = (int32_t)(demand[n] < capacity ? demand[n] : capacity);
+        offsets[n + 1] = offsets[n] + counts[n];
+    }
+    int64_t dropped = 0;
+    for (int n = 0; n < N; ++n) demand[n] = 0;          /* reused: assignments seen so far */
+    for (int64_t f = 0; f < A; ++f) {
+        int e = topk_idx[f];
+        int64_t r = demand[e]++;
+        if (r < capacity) {
+            int32_t row = offsets[e] + (int32_t)r;
+            perm[row] = (int32_t)(f / k);
+            inv_perm[f] = row;
+        } else {
+            inv_perm[f] = -2;
+            dropped += 1;
+        }
+    }
+    free(demand);
+    return dropped;
+}
+
 /* SiLU and tanh-GELU, [P3] s3.1 (SiLU(gate) * up). */
 static double silu(double v) { return v / (1.0 + exp(-v)); }
 static double gelu_tanh(double v)
@@ -285,7 +337,8 @@ int oracle_expert_rows(int64_t n_rows, int d, int F, int act,
 
 /* ---------------------------------------------------------------------------
  * Combine: [P2] s2.4, [P3] s2.2 / s5.1 step 5.
- *   out[t] = sum_{j<k} w[t,j] * y_perm[inv_perm[t*k+j]]   (j in order)
+ *   out[t] = sum_{j<k} w[t,j] * y_perm[inv_perm[t*k+j]]   (j in order;
+ *            assignments dropped by a capacity limit, inv_perm < 0, add nothing)
  * Only the listed tokens (or all T when tokens == NULL) are written; out rows
  * are [n_tok, d] in the order of the list.
  * ------------------------------------------------------------------------- */
@@ -297,6 +350,7 @@ int oracle_combine(int64_t n_tok, const int64_t *tokens, int d, int k,
         int64_t t = tokens ? tokens[q] : q;
         for (int o = 0; o < d; ++o) out[q * d + o] = 0.0;
         for (int j = 0; j < k; ++j) {
+            if (inv_perm[t * k + j] < 0) continue;      /* dropped by a capacity limit */
             double w = topk_w[t * k + j];
             const double *yr = y_perm + (int64_t)inv_perm[t * k + j] * d;
             for (int o = 0; o < d; ++o) out[q * d + o] += w * yr[o];

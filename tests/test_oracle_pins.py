@@ -392,3 +392,62 @@ def test_fp32_decisions_differ_from_exact_only_on_uncertified_tokens():
         assert np.all(same[r64["cert"] > 0])
         assert same.mean() > 0.99
         np.testing.assert_array_equal(r32["cert"], r64["cert"])
+
+
+# ---------------------------------------------------------------- capacity / token drop
+def test_capacity_formula_on_the_worked_example():
+    """capacity = capacity_factor * total / num_experts (rounded up), with total
+    = T*k assignments: 16384 / 64 = 256 at 1.0, 320 at 1.25."""
+    g = GOLD["capacity"]
+    T, N, k = 8192, g["worked_example_experts"], 2
+    assert T * k == g["worked_example_assignments"]
+    assert oracle.capacity(T, N, k, 1.0) == g["capacity_at_1_0"]
+    assert oracle.capacity(T, N, k, 1.25) == g["capacity_at_1_25"]
+    assert oracle.capacity(10, 3, 1, 1.0) == 4            # ceil(10/3)
+
+
+@pytest.mark.parametrize("T,N,k,cap", [(40, 5, 2, 10), (200, 8, 3, 50), (97, 16, 4, 1), (30, 4, 2, 0)])
+def test_capacity_keeps_the_earliest_assignments(T, N, k, cap):
+    """Each expert keeps its first `cap` assignments in flat order (a stable
+    sort by expert, then the head of every group); counts = min(demand, cap),
+    offsets their cumulative sum, dropped = the rest."""
+    rng = np.random.default_rng(T + cap)
+    skew = np.arange(1, N + 1, dtype=np.float64) ** -1.5
+    idx = np.stack([rng.choice(N, k, replace=False, p=skew / skew.sum()) for _ in range(T)]).astype(np.int32)
+    r = oracle.permute_capacity(idx, N, cap)
+    flat = idx.reshape(-1)
+    demand = np.bincount(flat, minlength=N)
+    np.testing.assert_array_equal(r["counts"], np.minimum(demand, cap))
+    np.testing.assert_array_equal(r["offsets"], np.concatenate([[0], np.cumsum(np.minimum(demand, cap))]))
+    assert r["dropped"] == int(np.maximum(demand - cap, 0).sum())
+    assert int(r["counts"].sum()) + r["dropped"] == T * k
+    order = np.argsort(flat, kind="stable")                # flat assignments grouped by expert
+    group_start = np.concatenate([[0], np.cumsum(demand)])
+    kept_rows = []
+    for e in range(N):
+        kept_rows += list(order[group_start[e]:group_start[e] + min(demand[e], cap)])
+    kept_rows = np.array(kept_rows, dtype=np.int64)
+    np.testing.assert_array_equal(r["perm"], kept_rows // k)
+    inv = np.full(T * k, -2)
+    inv[kept_rows] = np.arange(len(kept_rows))
+    np.testing.assert_array_equal(r["inv_perm"], inv)
+
+
+def test_capacity_at_or_above_demand_is_the_plain_grouping():
+    idx = _random_routing(150, 6, 2, 5)
+    big = oracle.permute_capacity(idx, 6, 10 ** 6)
+    plain = oracle.permute(idx, 6)
+    assert big["dropped"] == 0
+    for key in ("counts", "offsets", "perm", "inv_perm"):
+        np.testing.assert_array_equal(big[key], plain[key])
+
+
+def test_dropped_assignment_adds_nothing_to_the_output():
+    """Token A of the pages' example (experts 0 and 3, weights 0.7 / 0.3): if
+    expert 3 is over capacity, the layer output is 0.7 * E0(x) alone (no
+    renormalisation); with capacity 0 the output is zero."""
+    y = np.array([[2.0], [5.0]])                     # rows: E0(x) for token 0, E3(x) for token 0
+    w = np.array([[0.7, 0.3]])
+    assert oracle.combine(y, np.array([0, -2], np.int32), w)[0, 0] == pytest.approx(0.7 * 2.0)
+    assert oracle.combine(y, np.array([-2, -2], np.int32), w)[0, 0] == 0.0
+    assert oracle.combine(y, np.array([0, 1], np.int32), w)[0, 0] == pytest.approx(0.7 * 2.0 + 0.3 * 5.0)

@@ -225,6 +225,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens"],
                     help="tensor-core tiling of the grouped GEMMs (library default: auto)")
+    ap.add_argument("--capacity-factor", type=float, default=None,
+                    help="expert capacity ceil(cf * T * k / N); overflow assignments are dropped")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w0 = S.WORKLOADS[args.workload]
@@ -287,6 +289,8 @@ def main():
     xp = torch.empty((A, w.d), dtype=td, device="cuda")
     yp = torch.empty((A, w.d), dtype=td, device="cuda")
     out = torch.empty((w.T, w.d), dtype=td, device="cuda")
+    dropped = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cf = args.capacity_factor
     ws = B.workspace(max(B.permute_workspace_size(s), B.grouped_ffn_workspace_size(s)))
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
@@ -295,7 +299,10 @@ def main():
         if ev: ev[0].record(stream)
         B.route(s, x, wg, bias, idx, tw)
         if ev: ev[1].record(stream)
-        B.permute(s, idx, x, counts, offsets, perm, inv, xp, ws)
+        if cf is None:
+            B.permute(s, idx, x, counts, offsets, perm, inv, xp, ws)
+        else:
+            B.permute_capacity(s, idx, x, cf, counts, offsets, perm, inv, xp, ws, dropped=dropped)
         if ev: ev[2].record(stream)
         B.grouped_ffn(s, xp, offsets, WG, WU, WD, yp, ws)
         if ev: ev[3].record(stream)
@@ -336,8 +343,17 @@ def main():
         out_host = torch.empty((w.T, w.d), dtype=td).pin_memory()
         wsh = B.workspace(B.hostio_workspace_size(s))
         del ws
+
+        def forward_e2e():
+            if cf is None:
+                B.forward_hostio(s, x_host, wg, bias, WG, WU, WD, out_host, wsh)
+            else:                              # no host-buffer entry with a capacity: copies around the call
+                x.copy_(x_host, non_blocking=True)
+                B.forward_capacity(s, cf, x, wg, bias, WG, WU, WD, out, wsh)
+                out_host.copy_(out, non_blocking=True)
+
         for _ in range(2):
-            B.forward_hostio(s, x_host, wg, bias, WG, WU, WD, out_host, wsh)
+            forward_e2e()
         torch.cuda.synchronize()
         e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps)]
@@ -346,7 +362,7 @@ def main():
         for i in range(args.steps):
             flush.zero_()
             e_ev[i][0].record(stream)
-            B.forward_hostio(s, x_host, wg, bias, WG, WU, WD, out_host, wsh)
+            forward_e2e()
             e_ev[i][1].record(stream)
         torch.cuda.synchronize()
         if B.get_error() != B.MOE_OK:
@@ -364,12 +380,13 @@ def main():
 
     P = peaks()
     cnt = counts.cpu().numpy()
-    up_f, down_f = acc.up_flops(A, w.d, w.F, w.act), acc.down_flops(A, w.d, w.F)
+    rows = int(cnt.sum())                      # rows the grouped FFN computed (A unless a capacity dropped some)
+    up_f, down_f = acc.up_flops(rows, w.d, w.F, w.act), acc.down_flops(rows, w.d, w.F)
     ffn_flops = up_f + down_f
     wbytes = acc.active_expert_weight_bytes(cnt, w.d, w.F, w.act, w.esize)
     # prefill-shaped (many rows per active expert): tensor roofline; decode-shaped: the HBM bytes of the
     # active experts' weights. Both fractions are reported.
-    rows_per_active = A / max(1, int((cnt > 0).sum()))
+    rows_per_active = rows / max(1, int((cnt > 0).sum()))
     tensor_bound = rows_per_active >= 128
     traffic = recorded_traffic(w.name)
     tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
@@ -403,13 +420,14 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,
-                   "gate": "fp32", "ffn_tiling": args.ffn_tiling, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "gate": "fp32", "ffn_tiling": args.ffn_tiling, "capacity_factor": cf, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write); expert weights also exceed L2"},
         "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
         "stage_ms": {"route": float(stage[:, 0].mean()), "permute": float(stage[:, 1].mean()),
                      "grouped_ffn": ffn_ms, "combine": float(stage[:, 3].mean())},
         "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()),
+        "dropped_assignments": int(dropped.item()) if cf is not None else 0,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": 8 * args.steps,   # route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1
         "clocks": clocks,

@@ -101,11 +101,13 @@ moe_status moe_permute(const moe_shape *s, const int32_t *topk_idx, const void *
  * "MoE显存与计算开销四阶段手算指南" sections 2.3 and 4.3 (one launch over
  * all experts, inputs contiguous, expert_offsets).
  * For MOE_GELU_TANH: h = gelu_tanh(x W_1^T), y = h W_2^T (w_up = NULL).
- * x_perm [A,d], offsets [N+1] (as from moe_permute), y_perm [A,d].
+ * x_perm [A,d], offsets [N+1] (as from moe_permute / moe_permute_capacity:
+ * rows offsets[N] .. A-1 are ignored), y_perm [A,d].
  * bf16: tcgen05 tensor cores, fp32 accumulation in tensor memory, h rounded
  * to bf16; f32: fp32 CUDA-core GEMM. ws: moe_grouped_ffn_workspace_size(s)
- * bytes (holds h). Offsets that are not a monotone partition of [0, A)
- * record MOE_ERR_CORRUPT and the GEMMs do nothing.
+ * bytes (holds h). Offsets that are not a monotone partition of a prefix
+ * [0, offsets[N]) of the A rows record MOE_ERR_CORRUPT and the GEMMs do
+ * nothing.
  */
 moe_status moe_grouped_ffn(const moe_shape *s, const void *x_perm, const int32_t *offsets,
                            const void *w_gate, const void *w_up, const void *w_down,
@@ -132,6 +134,31 @@ moe_status moe_forward(const moe_shape *s, const void *x, const float *w_g, cons
                        const void *w_gate, const void *w_up, const void *w_down, void *out,
                        int32_t *topk_idx, float *topk_w, int32_t *counts,
                        void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Grouping with an expert capacity: "MoE混合专家模型计算原理与推理部署实战解析"
+ * section 4.3 (at inference an expert takes at most
+ * capacity_factor * total_tokens / num_experts tokens; the overflow is dropped
+ * and only the residual path carries it). Here the capacity is
+ * ceil(capacity_factor * T * k / N) assignments per expert; an expert keeps
+ * its earliest assignments in flat order t*k + j. Outputs as moe_permute,
+ * except: counts / offsets describe the kept rows (offsets[N] <= T*k),
+ * inv_perm[f] = -2 for a dropped assignment, and *dropped (optional, int32)
+ * receives the number of dropped assignments. moe_grouped_ffn and
+ * moe_combine accept these directly (a dropped assignment adds nothing to
+ * the token's output; kept gate weights are not renormalised).
+ */
+moe_status moe_permute_capacity(const moe_shape *s, const int32_t *topk_idx, const void *x,
+                                double capacity_factor, int32_t *counts, int32_t *offsets,
+                                int32_t *perm, int32_t *inv_perm, void *x_perm, int32_t *dropped,
+                                void *ws, size_t ws_bytes, void *stream);
+
+/* moe_forward with an expert capacity (see moe_permute_capacity); ws as moe_forward. */
+moe_status moe_forward_capacity(const moe_shape *s, double capacity_factor, const void *x,
+                                const float *w_g, const float *bias, const void *w_gate,
+                                const void *w_up, const void *w_down, void *out, int32_t *topk_idx,
+                                float *topk_w, int32_t *counts, int32_t *dropped, void *ws,
+                                size_t ws_bytes, void *stream);
 
 /*
  * moe_forward with x and out in HOST memory (pinned memory makes the copies

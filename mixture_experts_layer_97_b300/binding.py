@@ -40,6 +40,8 @@ SIGNATURES = {
     "moe_permute": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_grouped_ffn": (I32, [SP, P, P, P, P, P, P, P, SZ, P]),
     "moe_permute_noalloc": (I32, [SP, P, P, P, P, P, P, P, P]),
+    "moe_permute_capacity": (I32, [SP, P, P, ctypes.c_double, P, P, P, P, P, P, P, SZ, P]),
+    "moe_forward_capacity": (I32, [SP, ctypes.c_double, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_combine": (I32, [SP, P, P, P, P, P]),
     "moe_forward": (I32, [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_hostio": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
@@ -158,6 +160,22 @@ def permute_noalloc(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, str
     _check(lib().moe_permute_noalloc(ctypes.byref(s), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
                                      _ptr(perm), _ptr(inv_perm), _ptr(x_perm), _stream(stream)),
            "moe_permute_noalloc")
+
+
+def permute_capacity(s, topk_idx, x, capacity_factor, counts, offsets, perm, inv_perm, x_perm, ws, dropped=None,
+                     stream=None):
+    _check(lib().moe_permute_capacity(ctypes.byref(s), _ptr(topk_idx), _ptr(x), float(capacity_factor), _ptr(counts),
+                                      _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(x_perm), _ptr(dropped),
+                                      _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)),
+           "moe_permute_capacity")
+
+
+def forward_capacity(s, capacity_factor, x, w_g, bias, w_gate, w_up, w_down, out, ws, topk_idx=None, topk_w=None,
+                     counts=None, dropped=None, stream=None):
+    _check(lib().moe_forward_capacity(ctypes.byref(s), float(capacity_factor), _ptr(x), _ptr(w_g), _ptr(bias),
+                                      _ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx),
+                                      _ptr(topk_w), _ptr(counts), _ptr(dropped), _ptr(ws), ws.numel(),
+                                      _stream(stream)), "moe_forward_capacity")
 
 
 def grouped_ffn(s, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, stream=None):

@@ -3,6 +3,7 @@
 // "MoE显存与计算开销四阶段手算指南" section 2.4 and
 // "MoE混合专家模型计算原理与推理部署实战解析" sections 2.2 and 5.1 step 5:
 //   out[t,:] = sum_{j<k} w[t,j] * y_perm[inv_perm[t*k+j], :]
+// (an assignment dropped by an expert capacity, inv_perm = -2, adds nothing)
 // A flat grid of warps over (token, group of 16-byte column chunks): each
 // lane accumulates its chunks of the k gathered rows in fp32 in j order and
 // writes them once. No zero-fill and no atomics, so the result is bitwise
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __res
   for (int j = 0; j < k; ++j) {
     const int64_t row = inv_perm[t * k + j];
     const float w = topk_w[t * k + j];
+    if (row == -2) continue;   // dropped by the expert capacity: adds nothing
     if (row < 0 || row >= A) {
       if (c0 == 0) record_error(MOE_ERR_CORRUPT);
       continue;

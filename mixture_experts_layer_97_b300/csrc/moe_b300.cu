@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <type_traits>
@@ -196,19 +197,22 @@ moe_status route_impl(const moe_shape* s, const void* x, const float* wg, const 
 }
 
 // ---------------------------------------------------------------- permute
+constexpr long long kNoCapacity = 0x7fffffffffffffffLL;
+
 moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, int32_t* counts, int32_t* offsets,
-                        int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, cudaStream_t st) {
+                        int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, cudaStream_t st,
+                        long long capacity = kNoCapacity, int32_t* dropped = nullptr) {
   const int64_t C = perm_chunks(s);
   int32_t* hist = static_cast<int32_t*>(ws);
   if (C > 0) {
     permute_hist_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, s->T, s->N, s->k, hist);
     if (launched() != MOE_OK) return MOE_ERR_CUDA;
   }
-  permute_scan_kernel<<<1, 256, 0, st>>>(hist, static_cast<int>(C), s->N, counts, offsets);
+  permute_scan_kernel<<<1, 256, 0, st>>>(hist, static_cast<int>(C), s->N, capacity, counts, offsets, dropped);
   if (launched() != MOE_OK) return MOE_ERR_CUDA;
   if (C > 0) {
-    permute_rank_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, hist, s->T, s->N, s->k, perm,
-                                                                            inv_perm);
+    permute_rank_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, hist, offsets, s->T, s->N, s->k,
+                                                                            capacity, perm, inv_perm, dropped);
     if (launched() != MOE_OK) return MOE_ERR_CUDA;
     const int64_t nv = static_cast<int64_t>(s->d) * esize(s) / 16;
     const int64_t warps = s->T * copy_groups(nv);
@@ -217,6 +221,14 @@ moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, i
     if (launched() != MOE_OK) return MOE_ERR_CUDA;
   }
   return MOE_OK;
+}
+
+// Rows an expert keeps under a capacity factor: ceil(cf * T * k / N) ("MoE混合专家
+// 模型计算原理与推理部署实战解析" section 4.3, total counted in assignments).
+long long capacity_rows(const moe_shape* s, double capacity_factor) {
+  const double c = std::ceil(capacity_factor * static_cast<double>(s->T) * static_cast<double>(s->k) /
+                             static_cast<double>(s->N));
+  return c >= 2147483647.0 ? kNoCapacity : static_cast<long long>(c);
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -391,13 +403,14 @@ moe_status combine_impl(const moe_shape* s, const void* y_perm, const int32_t* i
 
 moe_status forward_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, const void* w_gate,
                         const void* w_up, const void* w_down, void* out, int32_t* topk_idx, float* topk_w,
-                        int32_t* counts, const FwdBufs& b, cudaStream_t st) {
+                        int32_t* counts, const FwdBufs& b, cudaStream_t st, long long capacity = kNoCapacity,
+                        int32_t* dropped = nullptr) {
   int32_t* idx = topk_idx ? topk_idx : b.topk_idx;
   float* w = topk_w ? topk_w : b.topk_w;
   int32_t* cnt = counts ? counts : b.counts;
   moe_status r = route_impl(s, x, wg, bias, idx, w, st);
   if (r != MOE_OK) return r;
-  r = permute_impl(s, idx, x, cnt, b.offsets, b.perm, b.inv_perm, b.x_perm, b.perm_ws, st);
+  r = permute_impl(s, idx, x, cnt, b.offsets, b.perm, b.inv_perm, b.x_perm, b.perm_ws, st, capacity, dropped);
   if (r != MOE_OK) return r;
   r = ffn_impl(s, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st);
   if (r != MOE_OK) return r;
@@ -465,6 +478,22 @@ moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const void* 
   return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, static_cast<cudaStream_t>(stream));
 }
 
+moe_status moe_permute_capacity(const moe_shape* s, const int32_t* topk_idx, const void* x, double capacity_factor,
+                                int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* x_perm,
+                                int32_t* dropped, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  if (!(capacity_factor >= 0.0)) return MOE_ERR_INVALID_ARG;
+  const bool any = s->T > 0;
+  if (!ptr_ok(topk_idx, any) || !ptr_ok(x, any) || !ptr_ok(counts, true) || !ptr_ok(offsets, true) ||
+      !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, any) || !ptr_ok(dropped, false) ||
+      !ptr_ok(ws, permute_ws(s) > 0))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < permute_ws(s)) return MOE_ERR_WORKSPACE;
+  return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, static_cast<cudaStream_t>(stream),
+                      capacity_rows(s, capacity_factor), dropped);
+}
+
 moe_status moe_grouped_ffn(const moe_shape* s, const void* x_perm, const int32_t* offsets, const void* w_gate,
                            const void* w_up, const void* w_down, void* y_perm, void* ws, size_t ws_bytes,
                            void* stream) {
@@ -502,6 +531,24 @@ moe_status moe_forward(const moe_shape* s, const void* x, const float* w_g, cons
   if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
   return forward_impl(s, x, w_g, bias, w_gate, w_up, w_down, out, topk_idx, topk_w, counts, b,
                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_capacity(const moe_shape* s, double capacity_factor, const void* x, const float* w_g,
+                                const float* bias, const void* w_gate, const void* w_up, const void* w_down,
+                                void* out, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* dropped,
+                                void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  if (!(capacity_factor >= 0.0)) return MOE_ERR_INVALID_ARG;
+  const bool any = s->T > 0;
+  if (!ptr_ok(x, any) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) || !weights_ok(s, w_gate, w_up, w_down) ||
+      !ptr_ok(out, any) || !ptr_ok(topk_idx, false) || !ptr_ok(topk_w, false) || !ptr_ok(counts, false) ||
+      !ptr_ok(dropped, false) || !ptr_ok(ws, true))
+    return MOE_ERR_INVALID_ARG;
+  const FwdBufs b = carve_forward(s, ws, false);
+  if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  return forward_impl(s, x, w_g, bias, w_gate, w_up, w_down, out, topk_idx, topk_w, counts, b,
+                      static_cast<cudaStream_t>(stream), capacity_rows(s, capacity_factor), dropped);
 }
 
 moe_status moe_forward_hostio(const moe_shape* s, const void* x_host, const float* w_g, const float* bias,

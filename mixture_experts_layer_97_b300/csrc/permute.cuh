@@ -10,10 +10,12 @@
 //   hist    per chunk of whole tokens (at most 2048 assignments): expert
 //           histogram (shared-memory integer atomics: counts do not depend
 //           on their order)
-//   scan    one CTA: counts, offsets, and the first row of every
+//   scan    one CTA: counts, offsets, and the rank base of every
 //           (chunk, expert) pair
 //   rank    per chunk: stable ranks from warp __match_any_sync + popc in flat
-//           order -> perm / inv_perm
+//           order -> perm / inv_perm; with an expert capacity ("MoE混合专家模型
+//           计算原理与推理部署实战解析" section 4.3) ranks >= capacity are
+//           dropped (inv_perm = -2) and counted
 //   copy    flat grid of warps over (token, 2 KB slice of its row): each warp
 //           reads its slice of x once with 128-bit loads and writes it to the
 //           token's k rows, so the copy spreads over every SM.
@@ -53,24 +55,29 @@ __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_
   for (int n = threadIdx.x; n < N; n += blockDim.x) hist[c * N + n] = h[n];
 }
 
-// Single CTA of 256 threads; thread n owns expert n.
+// Single CTA of 256 threads; thread n owns expert n. On return hist[c][n]
+// holds the number of expert n's assignments in chunks before c (its rank
+// base); counts / offsets describe the KEPT rows: min(demand, capacity) per
+// expert ("MoE混合专家模型计算原理与推理部署实战解析" section 4.3; capacity =
+// INT64_MAX keeps everything). *dropped (optional) is zeroed for the rank pass.
 __global__ void __launch_bounds__(256) permute_scan_kernel(int32_t* __restrict__ hist, int n_chunks, int N,
-                                                           int32_t* __restrict__ counts,
-                                                           int32_t* __restrict__ offsets) {
-  __shared__ int tot[256];
+                                                           long long capacity, int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ dropped) {
   __shared__ int warp_sums[8];
   const int n = threadIdx.x;
   int run = 0;
   if (n < N) {
     for (int c = 0; c < n_chunks; ++c) {
       const int v = hist[static_cast<int64_t>(c) * N + n];
-      hist[static_cast<int64_t>(c) * N + n] = run;   // chunk-local base, before the expert offset
+      hist[static_cast<int64_t>(c) * N + n] = run;   // rank base of chunk c within expert n
       run += v;
     }
   }
-  // exclusive scan of run over experts
+  const int kept = static_cast<int>(run < capacity ? run : capacity);
+  // exclusive scan of the kept counts over experts
   const int lane = n & 31, w = n >> 5;
-  int incl = run;
+  int incl = kept;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int o = __shfl_up_sync(0xffffffffu, incl, off);
@@ -80,23 +87,24 @@ __global__ void __launch_bounds__(256) permute_scan_kernel(int32_t* __restrict__
   __syncthreads();
   int wbase = 0;
   for (int i = 0; i < w; ++i) wbase += warp_sums[i];
-  const int excl = wbase + incl - run;
-  tot[n] = excl;
   if (n < N) {
-    counts[n] = run;
-    offsets[n] = excl;
+    counts[n] = kept;
+    offsets[n] = wbase + incl - kept;
   }
-  if (n == 255) offsets[N] = wbase + incl;   // total of valid assignments (T*k unless corrupt)
-  __syncthreads();
-  if (n < N) {
-    for (int c = 0; c < n_chunks; ++c) hist[static_cast<int64_t>(c) * N + n] += tot[n];
-  }
+  if (n == 255) offsets[N] = wbase + incl;   // kept rows (T*k when nothing is dropped or corrupt)
+  if (n == 0 && dropped != nullptr) *dropped = 0;
 }
 
+// Marker of an assignment dropped by the capacity limit in inv_perm.
+constexpr int32_t kDroppedRow = -2;
+
 __global__ void __launch_bounds__(kPermThreads) permute_rank_kernel(const int32_t* __restrict__ topk_idx,
-                                                                    const int32_t* __restrict__ base, int64_t T,
-                                                                    int N, int k, int32_t* __restrict__ perm,
-                                                                    int32_t* __restrict__ inv_perm) {
+                                                                    const int32_t* __restrict__ base,
+                                                                    const int32_t* __restrict__ offsets, int64_t T,
+                                                                    int N, int k, long long capacity,
+                                                                    int32_t* __restrict__ perm,
+                                                                    int32_t* __restrict__ inv_perm,
+                                                                    int32_t* __restrict__ dropped) {
   __shared__ int wh[kPermWarps][256];
   const int tpc = perm_tokens_per_chunk(k);
   const int64_t c = blockIdx.x;
@@ -122,7 +130,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_rank_kernel(const int32_
     __syncwarp();
   }
   __syncthreads();
-  // pass 2: per-expert prefix over warps, starting at the chunk's base row
+  // pass 2: per-expert prefix over warps, starting at the chunk's rank base
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
     int run = base[c * N + n];
 #pragma unroll
@@ -133,21 +141,36 @@ __global__ void __launch_bounds__(kPermThreads) permute_rank_kernel(const int32_
     }
   }
   __syncthreads();
-  // pass 3: stable ranks in flat order
+  // pass 3: stable ranks in flat order; rank >= capacity is dropped
+  int n_drop = 0;
   for (int g = s0; g < s1; g += 32) {
     const int fl = g + lane;
     int e = (fl < s1) ? topk_idx[f0 + fl] : -1;
     if (e >= N) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
-    int row = -1;
-    if (e >= 0) row = wh[warp][e] + __popc(peers & lt_mask);
+    int rank = -1;
+    if (e >= 0) rank = wh[warp][e] + __popc(peers & lt_mask);
     __syncwarp();
     if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
     __syncwarp();
     if (fl < s1) {
+      int row = -1;
+      if (e >= 0) {
+        if (rank < capacity) {
+          row = offsets[e] + rank;
+          perm[row] = static_cast<int32_t>((f0 + fl) / k);
+        } else {
+          row = kDroppedRow;
+          ++n_drop;
+        }
+      }
       inv_perm[f0 + fl] = row;
-      if (row >= 0) perm[row] = static_cast<int32_t>((f0 + fl) / k);
     }
+  }
+  if (dropped != nullptr) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) n_drop += __shfl_xor_sync(0xffffffffu, n_drop, off);
+    if (lane == 0 && n_drop > 0) atomicAdd(dropped, n_drop);   // integer: order-independent
   }
 }
 

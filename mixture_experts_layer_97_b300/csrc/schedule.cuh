@@ -13,7 +13,9 @@ namespace moe {
 
 // Called by all 32 lanes of one warp. Fills s_off[0..N] (a copy of offsets)
 // and s_pre[0..N] (prefix of ceil(rows / BM) over experts); *s_bad = 1 when
-// offsets are not a monotone partition of [0, rows_total).
+// offsets are not a monotone partition of a prefix [0, offsets[N]) of the
+// rows_total rows (offsets[N] < rows_total when an expert capacity dropped
+// assignments).
 __device__ inline void build_tile_prefix(const int32_t* __restrict__ offsets, int N, int rows_total, int BM,
                                          int* s_off, int* s_pre, int* s_bad) {
   const int lane = threadIdx.x & 31;
@@ -30,7 +32,7 @@ __device__ inline void build_tile_prefix(const int32_t* __restrict__ offsets, in
   if (lane == 0) {
     const int a0 = offsets[0], aN = offsets[N];
     s_off[N] = aN;
-    if (a0 != 0 || aN != rows_total) bad = true;
+    if (a0 != 0 || aN > rows_total) bad = true;
   }
   int incl = sum;
 #pragma unroll

@@ -113,7 +113,7 @@ def test_ffn_repeatable_bitwise(tiling):
 def test_ffn_corrupt_offsets_recorded(dtype, tiling):
     w, xp, ws, off = make_case([10, 20, 30], 128, 128, "swiglu", dtype, 0)
     bad = off.copy()
-    bad[3] = 59                                       # does not add up to A = 60
+    bad[3] = 61                                       # runs past the A = 60 rows
     s = B.shape(w.T, w.d, w.N, 1, w.F, w.act, w.dtype)
     stack = lambda i: dev(np.stack([ws[e][i] for e in range(w.N)]))
     y = new((w.T, w.d), dtype, fill=0)
@@ -121,6 +121,47 @@ def test_ffn_corrupt_offsets_recorded(dtype, tiling):
     B.grouped_ffn(s, dev(xp), dev(bad), stack(0), stack(1), stack(2), y, wsb)
     assert B.get_error() == B.MOE_ERR_CORRUPT
     assert float(y.float().abs().max()) == 0.0       # nothing written
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_ffn_non_monotone_offsets_recorded(dtype):
+    w, xp, ws, off = make_case([10, 20, 30], 128, 128, "swiglu", dtype, 0)
+    bad = np.array([0, 20, 10, 60], dtype=np.int32)
+    s = B.shape(w.T, w.d, w.N, 1, w.F, w.act, w.dtype)
+    stack = lambda i: dev(np.stack([ws[e][i] for e in range(w.N)]))
+    y = new((w.T, w.d), dtype, fill=0)
+    B.grouped_ffn(s, dev(xp), dev(bad), stack(0), stack(1), stack(2), y,
+                  B.workspace(B.grouped_ffn_workspace_size(s)))
+    assert B.get_error() == B.MOE_ERR_CORRUPT
+    assert float(y.float().abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_ffn_offsets_cover_a_prefix_of_the_rows(dtype, tiling):
+    """After a capacity drop the kept rows are a prefix [0, offsets[N]) of the
+    A-row buffers: those rows match the oracle and the tail is not written."""
+    counts = [40, 0, 129, 17]
+    w, xp, ws, off = make_case(counts, 256, 256, "swiglu", dtype, 5)
+    N = len(counts)
+    A = w.T
+    kept = off
+    extra = 50                                        # rows past offsets[N], never read or written
+    s = B.shape(A + extra, w.d, N, 1, w.F, w.act, w.dtype)
+    stack = lambda i: dev(np.stack([ws[e][i] for e in range(N)]))
+    x_full = np.concatenate([xp, xp[:extra]])
+    y = new((A + extra, w.d), dtype, fill=0)
+    y[A:] = 7
+    B.grouped_ffn(s, dev(x_full), dev(kept), stack(0), stack(1), stack(2), y,
+                  B.workspace(B.grouped_ffn_workspace_size(s)))
+    assert B.get_error() == B.MOE_OK
+    got = host_f64(y)
+    ref = np.zeros((A, w.d))
+    for e in range(N):
+        a, b = kept[e], kept[e + 1]
+        if b > a:
+            ref[a:b] = oracle.expert_rows(xp[a:b], *ws[e], w.act)
+    assert rel_err(got[:A], ref) <= tol(dtype)
+    assert np.all(got[A:] == 7)
 
 
 def test_tilings_agree_within_tolerance():

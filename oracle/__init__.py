@@ -53,7 +53,7 @@ def lib():
         L = ctypes.CDLL(_LIB)
         P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.oracle_num_threads.restype = I
-        L.oracle_route.argtypes = [I64, I, I, I, P, I, P, I, P, I, I, P, P, P, P, P]
+        L.oracle_route.argtypes = [I64, I, I, I, P, I, P, I, P, I, I, I, P, P, P, P, P, P]
         L.oracle_route.restype = I
         L.oracle_permute.argtypes = [I64, I, I, P, P, P, P, P]
         L.oracle_permute.restype = I
@@ -65,7 +65,9 @@ def lib():
         L.oracle_expert_rows.restype = I
         L.oracle_combine.argtypes = [I64, P, I, I, P, P, P, P]
         L.oracle_combine.restype = I
-        L.oracle_forward.argtypes = [I64, I, I, I, I, I, P, I, P, I, P, I, I, P, P, P, I,
+        L.oracle_load_stats.argtypes = [I64, I, I, P, P, P, P, P]
+        L.oracle_load_stats.restype = I
+        L.oracle_forward.argtypes = [I64, I, I, I, I, I, P, I, P, I, P, I, I, I, P, P, P, I,
                                      P, P, P, P, P, P, P, P, P]
         L.oracle_forward.restype = I
         _lib = L
@@ -96,13 +98,19 @@ def _p(a):
     return None if a is None else a.ctypes.data
 
 
-def route(x, wg, k, bias=None, want_logits=False, gate="fp32"):
+BIAS_MODES = {"logits": 0, "select": 1}
+
+
+def route(x, wg, k, bias=None, want_logits=False, gate="fp32", bias_mode="logits", want_probs=False):
     """Gate -> softmax -> top-k -> renormalise for every row of x.
 
     gate="fp32" (the pages' precision for the gate) takes the top-k decision
     on the fp32 logits of the sequential FMA chain; gate="fp64" on exact
-    logits. Returns dict(topk_idx [T,k] int32, topk_w [T,k] f64, cert [T],
-    errb [T,N] (both about the exact logits), and logits [T,N] when asked)."""
+    logits. bias_mode="logits" adds the bias to the logits before the
+    softmax; "select" adds it only to the scores that choose the experts.
+    Returns dict(topk_idx [T,k] int32, topk_w [T,k] f64, cert [T], errb [T,N]
+    (both about the exact scores), and logits [T,N] (the scores) / probs
+    [T,N] (the softmax) when asked)."""
     x, wg, bias = _c(x), _c(wg), _c(bias)
     T, d = x.shape
     N = wg.shape[1]
@@ -111,14 +119,33 @@ def route(x, wg, k, bias=None, want_logits=False, gate="fp32"):
     cert = np.empty((T,), np.float64)
     errb = np.empty((T, N), np.float64)
     logits = np.empty((T, N), np.float64) if want_logits else None
-    rc = lib().oracle_route(T, d, N, k, _p(x), _dt(x), _p(wg), _dt(wg), _p(bias), _dt(bias),
-                            1 if gate == "fp32" else 0, _p(idx), _p(w), _p(logits), _p(errb), _p(cert))
+    probs = np.empty((T, N), np.float64) if want_probs else None
+    rc = lib().oracle_route(T, d, N, k, _p(x), _dt(x), _p(wg), _dt(wg), _p(bias), _dt(bias), BIAS_MODES[bias_mode],
+                            1 if gate == "fp32" else 0, _p(idx), _p(w), _p(logits), _p(errb), _p(cert), _p(probs))
     if rc:
         raise ValueError("oracle_route: bad arguments")
     out = dict(topk_idx=idx, topk_w=w, cert=cert, errb=errb)
     if want_logits:
         out["logits"] = logits
+    if want_probs:
+        out["probs"] = probs
     return out
+
+
+def load_stats(probs, topk_idx):
+    """Routing statistics of one batch: f [N] (fraction of assignments per
+    expert), P [N] (mean gate probability), balance = N * sum f*P, entropy
+    (bits) of f, top1 = mean max probability."""
+    probs = np.ascontiguousarray(probs, dtype=np.float64)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, N = probs.shape
+    k = idx.shape[1] if idx.ndim == 2 else 1
+    f = np.empty(N, np.float64)
+    P = np.empty(N, np.float64)
+    o = np.empty(3, np.float64)
+    if lib().oracle_load_stats(T, N, k, _p(probs), _p(idx), _p(f), _p(P), _p(o)):
+        raise ValueError("oracle_load_stats: expert index out of range")
+    return dict(f=f, P=P, balance=float(o[0]), entropy_bits=float(o[1]), top1=float(o[2]))
 
 
 def permute(topk_idx, N):
@@ -185,7 +212,7 @@ def combine(y_perm, inv_perm, topk_w, tokens=None):
     return out
 
 
-def forward(x, wg, bias, w_gate, w_up, w_down, k, act, gate="fp32"):
+def forward(x, wg, bias, w_gate, w_up, w_down, k, act, gate="fp32", bias_mode="logits"):
     """The whole layer: route -> permute -> per-expert FFN -> combine."""
     x, wg, bias, w_gate, w_up, w_down = map(_c, (x, wg, bias, w_gate, w_up, w_down))
     T, d = x.shape
@@ -198,7 +225,7 @@ def forward(x, wg, bias, w_gate, w_up, w_down, k, act, gate="fp32"):
              inv_perm=np.empty(A, np.int32), y_perm=np.empty((A, d), np.float64),
              out=np.empty((T, d), np.float64))
     rc = lib().oracle_forward(T, d, N, k, F, ACTS[act], _p(x), _dt(x), _p(wg), _dt(wg), _p(bias), _dt(bias),
-                              1 if gate == "fp32" else 0, _p(w_gate), _p(w_up), _p(w_down), _dt(w_gate),
+                              BIAS_MODES[bias_mode], 1 if gate == "fp32" else 0, _p(w_gate), _p(w_up), _p(w_down), _dt(w_gate),
                               _p(r["topk_idx"]), _p(r["topk_w"]), _p(r["cert"]), _p(r["counts"]),
                               _p(r["offsets"]), _p(r["perm"]), _p(r["inv_perm"]), _p(r["y_perm"]),
                               _p(r["out"]))

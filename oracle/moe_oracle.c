@@ -17,6 +17,9 @@
  *        s2.3 grouping of tokens per expert (N_i, sum N_i = B*S*k),
  *        s2.4 weighted sum of the k expert outputs back in token order,
  *        s3 the toy forward (stacked per-expert inputs, per-expert Linear).
+ *   [P4] "这不是“参数越多越强”的简单故事" (deployment notes): s3.1 / s4.4
+ *        expert activation entropy and top-1 confidence as routing health
+ *        statistics.
  *   [P3] "MoE混合专家模型计算原理与推理部署实战解析": s2.1 gate, softmax, top-k;
  *        s2.2 renormalisation g_i' = g_i / sum of selected g and the weighted
  *        output; s2.4 gate kept in fp32; s3.1 SwiGLU expert
@@ -35,7 +38,11 @@
  *     false ties that rounded probabilities can create;
  *   - equal scores: the lower expert id wins; the k slots are in descending
  *     score order;
- *   - the bias (when given) is added to the logits before the softmax;
+ *   - the bias (when given) is added to the logits before the softmax
+ *     (bias_mode 0), or, as the auxiliary-loss-free balancing of [P3] s4.4
+ *     describes it, only to the scores that choose the experts
+ *     (bias_mode 1): then the gate weights come from the softmax of the
+ *     logits without the bias;
  *   - rows of one expert are kept in flat assignment order t*k + j (stable);
  *   - the two-matrix FFN uses the tanh form of GELU; no biases anywhere;
  *   - weights are stored [out, in].
@@ -73,12 +80,15 @@ int oracle_num_threads(void)
 
 /* ---------------------------------------------------------------------------
  * Route: [P2] s2.1-2.2, [P3] s2.1-2.2, s2.4.
- *   l[t,n] = sum_i x[t,i] * W_g[i,n] (+ b[n])   in fp32 when gate_fp32 != 0
- *            (sequential FMA chain in index order, then + b in fp32),
- *            else exactly in fp64
+ *   g[t,n] = sum_i x[t,i] * W_g[i,n]            in fp32 when gate_fp32 != 0
+ *            (sequential FMA chain in index order), else exactly in fp64
+ *   s[t,n] = g[t,n] + b[n]   (fp32 addition when gate_fp32; s = g without bias)
+ *   bias_mode 0: l = s    the bias is part of the logits
+ *   bias_mode 1: l = g    the bias only chooses ([P3] s4.4)
  *   p[t,:] = softmax(l[t,:])
- *   top-k by l (ties -> lower id), in descending order
+ *   top-k by s (ties -> lower id), in descending order
  *   w[t,j] = p[t,e_j] / sum_j' p[t,e_j']
+ *   probs   optional [T,N] copy of p
  *
  * Also returns, per token, how fragile the decision is against rounding
  * (computed from the exact fp64 logits whatever gate_fp32 says):
@@ -87,34 +97,35 @@ int oracle_num_threads(void)
  *              u = 2^-24 (the classical bound for a sum of d rounded products
  *              plus one rounded bias addition);
  *   cert[t]    min over i < k, j > i (sorted exact order) of
- *              (l_(i) - errb_(i)) - (l_(j) + errb_(j)) on the exact logits.
+ *              (s_(i) - errb_(i)) - (s_(j) + errb_(j)) on the exact scores.
  *              cert > 0 proves that ANY fp32 evaluation selects the same
  *              experts in the same order as exact arithmetic.
- *   logits     optional [T,N] copy of l (the fp32 values when gate_fp32).
+ *   logits     optional [T,N] copy of the scores s (fp32 values when gate_fp32).
  * Returns 0, or -1 on bad arguments.
  * ------------------------------------------------------------------------- */
 int oracle_route(int64_t T, int d, int N, int k,
                  const void *x, int x_dt,
                  const void *wg, int wg_dt,
-                 const void *bias, int b_dt, int gate_fp32,
+                 const void *bias, int b_dt, int bias_mode, int gate_fp32,
                  int32_t *topk_idx, double *topk_w,
-                 double *logits, double *errb, double *cert)
+                 double *logits, double *errb, double *cert, double *probs)
 {
-    if (T < 0 || d < 1 || N < 1 || k < 1 || k > N) return -1;
+    if (T < 0 || d < 1 || N < 1 || k < 1 || k > N || bias_mode < 0 || bias_mode > 1) return -1;
     const double u = ldexp(1.0, -24);
     const double gam = (d + 2) * u / (1.0 - (d + 2) * u);
     int bad = 0;
 
 #pragma omp parallel
     {
-        double *l = (double *)malloc(sizeof(double) * N);
+        double *l = (double *)malloc(sizeof(double) * N);   /* scores: choose the experts */
+        double *g = (double *)malloc(sizeof(double) * N);   /* logits of the softmax */
         double *s = (double *)malloc(sizeof(double) * N);
         double *p = (double *)malloc(sizeof(double) * N);
         double *eb = (double *)malloc(sizeof(double) * N);
         double *ex = (double *)malloc(sizeof(double) * N);
         int *taken = (int *)malloc(sizeof(int) * N);
         int *order = (int *)malloc(sizeof(int) * N);
-        if (!l || !s || !p || !eb || !ex || !taken || !order) {
+        if (!l || !g || !s || !p || !eb || !ex || !taken || !order) {
 #pragma omp atomic write
             bad = 1;
         } else {
@@ -134,15 +145,17 @@ int oracle_route(int64_t T, int d, int N, int k,
                     double b = bias ? rd(bias, b_dt, n) : 0.0;
                     ex[n] = acc + b;
                     l[n] = gate_fp32 ? (double)(bias ? acc32 + (float)b : acc32) : acc + b;
+                    g[n] = bias_mode == 1 ? (gate_fp32 ? (double)acc32 : acc) : l[n];
                     s[n] = aabs + fabs(b);
                     eb[n] = gam * s[n];
                 }
                 /* softmax over all N experts, with max subtraction */
-                double m = l[0];
-                for (int n = 1; n < N; ++n) if (l[n] > m) m = l[n];
+                double m = g[0];
+                for (int n = 1; n < N; ++n) if (g[n] > m) m = g[n];
                 double z = 0.0;
-                for (int n = 0; n < N; ++n) { p[n] = exp(l[n] - m); z += p[n]; }
+                for (int n = 0; n < N; ++n) { p[n] = exp(g[n] - m); z += p[n]; }
                 for (int n = 0; n < N; ++n) p[n] /= z;
+                if (probs) for (int n = 0; n < N; ++n) probs[t * N + n] = p[n];
                 /* full descending order by (l desc, id asc): repeated argmax */
                 for (int n = 0; n < N; ++n) taken[n] = 0;
                 for (int r = 0; r < N; ++r) {
@@ -187,7 +200,7 @@ int oracle_route(int64_t T, int d, int N, int k,
                 }
             }
         }
-        free(l); free(s); free(p); free(eb); free(ex); free(taken); free(order);
+        free(l); free(g); free(s); free(p); free(eb); free(ex); free(taken); free(order);
     }
     return bad ? -1 : 0;
 }
@@ -275,6 +288,55 @@ int64_t oracle_permute_capacity(int64_t T, int N, int k, const int32_t *topk_idx
     }
     free(demand);
     return dropped;
+}
+
+/* ---------------------------------------------------------------------------
+ * Load statistics of one routed batch: [P3] s4.2 (the Switch load-balance
+ * quantity) and [P4] "这不是“参数越多越强”的简单故事" s3.1 (expert activation
+ * entropy, maximum 4.0 for 16 experts) and s4.4 (monitoring: activation
+ * entropy, top-1 routing confidence).
+ *   f[n] = (number of assignments to n) / (T*k)          fraction routed to n
+ *   P[n] = (1/T) sum_t p[t,n]                            mean gate probability
+ *   out3[0] = N * sum_n f[n] * P[n]                      balance quantity (1 when uniform)
+ *   out3[1] = -sum_{f[n] > 0} f[n] log2 f[n]             activation entropy, bits (max log2 N)
+ *   out3[2] = (1/T) sum_t max_n p[t,n]                   mean top-1 probability
+ * p is the softmax whose values weight the experts (probs of oracle_route).
+ * Readings: f counts the k assignments of a token each (so sum f = 1 for any
+ * k, and uniform routing gives f = 1/N as the page's example needs); the
+ * entropy is in bits, as the page's "maximum 4.0 for 16 experts" implies; an
+ * empty batch gives all zeros. Returns 0, or -1 on a bad index.
+ * ------------------------------------------------------------------------- */
+int oracle_load_stats(int64_t T, int N, int k, const double *probs, const int32_t *topk_idx,
+                      double *f, double *P, double *out3)
+{
+    for (int n = 0; n < N; ++n) { f[n] = 0.0; P[n] = 0.0; }
+    out3[0] = out3[1] = out3[2] = 0.0;
+    if (T == 0) return 0;
+    for (int64_t a = 0; a < T * k; ++a) {
+        int e = topk_idx[a];
+        if (e < 0 || e >= N) return -1;
+        f[e] += 1.0;
+    }
+    for (int n = 0; n < N; ++n) f[n] /= (double)(T * k);
+    double conf = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        double mx = probs[t * N];
+        for (int n = 0; n < N; ++n) {
+            P[n] += probs[t * N + n];
+            if (probs[t * N + n] > mx) mx = probs[t * N + n];
+        }
+        conf += mx;
+    }
+    double bal = 0.0, ent = 0.0;
+    for (int n = 0; n < N; ++n) {
+        P[n] /= (double)T;
+        bal += f[n] * P[n];
+        if (f[n] > 0.0) ent -= f[n] * log2(f[n]);
+    }
+    out3[0] = (double)N * bal;
+    out3[1] = ent;
+    out3[2] = conf / (double)T;
+    return 0;
 }
 
 /* SiLU and tanh-GELU, [P3] s3.1 (SiLU(gate) * up). */
@@ -366,14 +428,16 @@ int oracle_combine(int64_t n_tok, const int64_t *tokens, int d, int k,
  * out [T, d] fp64. Routing outputs as in oracle_route / oracle_permute.
  * ------------------------------------------------------------------------- */
 int oracle_forward(int64_t T, int d, int N, int k, int F, int act,
-                   const void *x, int x_dt, const void *wg, int wg_dt, const void *bias, int b_dt, int gate_fp32,
+                   const void *x, int x_dt, const void *wg, int wg_dt, const void *bias, int b_dt, int bias_mode,
+                   int gate_fp32,
                    const void *w_gate, const void *w_up, const void *w_down, int w_dt,
                    int32_t *topk_idx, double *topk_w, double *cert,
                    int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                    double *y_perm, double *out)
 {
     const int64_t A = T * k;
-    int rc = oracle_route(T, d, N, k, x, x_dt, wg, wg_dt, bias, b_dt, gate_fp32, topk_idx, topk_w, NULL, NULL, cert);
+    int rc = oracle_route(T, d, N, k, x, x_dt, wg, wg_dt, bias, b_dt, bias_mode, gate_fp32, topk_idx, topk_w, NULL,
+                          NULL, cert, NULL);
     if (rc) return rc;
     rc = oracle_permute(T, N, k, topk_idx, counts, offsets, perm, inv_perm);
     if (rc) return rc;

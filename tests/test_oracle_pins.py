@@ -451,3 +451,134 @@ def test_dropped_assignment_adds_nothing_to_the_output():
     assert oracle.combine(y, np.array([0, -2], np.int32), w)[0, 0] == pytest.approx(0.7 * 2.0)
     assert oracle.combine(y, np.array([-2, -2], np.int32), w)[0, 0] == 0.0
     assert oracle.combine(y, np.array([0, 1], np.int32), w)[0, 0] == pytest.approx(0.7 * 2.0 + 0.3 * 5.0)
+
+
+# ---------------------------------------------------------------- selection-only bias / load statistics
+def _one_hot_gate(logit_rows):
+    """x = identity rows, so the logits are exactly the rows of W_g."""
+    g = np.asarray(logit_rows, dtype=np.float64)
+    return np.eye(g.shape[0]), g
+
+
+def test_selection_only_bias_hand_case():
+    """A bias that flips the choice: logits ln .5, ln .3, ln .2 and bias
+    (0, 0, 10), top-2. Both modes choose experts 2 and 0; selection-only
+    weights are .2/.7 and .5/.7, bias-in-logits weights come from
+    softmax(l + b) restricted to the pair."""
+    x, wg = _one_hot_gate([[math.log(.5), math.log(.3), math.log(.2)]])
+    b = np.array([0.0, 0.0, 10.0])
+    sel = oracle.route(x, wg, 2, bias=b, gate="fp64", bias_mode="select")
+    lgt = oracle.route(x, wg, 2, bias=b, gate="fp64", bias_mode="logits")
+    assert sel["topk_idx"].tolist() == [[2, 0]] and lgt["topk_idx"].tolist() == [[2, 0]]
+    np.testing.assert_allclose(sel["topk_w"][0], [.2 / .7, .5 / .7], rtol=1e-14)
+    e10 = math.exp(10.0)
+    np.testing.assert_allclose(lgt["topk_w"][0], [.2 * e10 / (.2 * e10 + .5), .5 / (.2 * e10 + .5)], rtol=1e-14)
+    assert "4.4" in GOLD["selection_only_bias"]["_cite"]   # the reading pinned here, with its citation
+
+
+def test_selection_only_bias_matches_its_definition():
+    """Selection by argsort of x@W_g + b (stable: lower id first on ties),
+    weights = softmax(x@W_g) over the chosen experts, renormalised (matmul,
+    stable sort and scipy's softmax as the independent routines)."""
+    T, d, N, k = 60, 12, 9, 3
+    x = _rand((T, d), 71)
+    wg = _rand((d, N), 72, 0.5)
+    b = _rand((N,), 73, 2.0)
+    r = oracle.route(x, wg, k, bias=b, gate="fp64", bias_mode="select", want_probs=True)
+    g = x @ wg
+    order = np.argsort(-(g + b), axis=1, kind="stable")[:, :k]
+    np.testing.assert_array_equal(r["topk_idx"], order)
+    p = special.softmax(g, axis=1)
+    np.testing.assert_allclose(r["probs"], p, rtol=1e-12)
+    sel = np.take_along_axis(p, order, 1)
+    np.testing.assert_allclose(r["topk_w"], sel / sel.sum(1, keepdims=True), rtol=1e-12)
+    # the bias-in-logits mode differs on this input (the pin separates the modes)
+    r2 = oracle.route(x, wg, k, bias=b, gate="fp64", bias_mode="logits", want_probs=True)
+    np.testing.assert_allclose(r2["probs"], special.softmax(g + b, axis=1), rtol=1e-12)
+    assert not np.allclose(r2["topk_w"], r["topk_w"])
+
+
+def test_selection_only_bias_invariances():
+    """Zero bias is the plain route; adding one constant to every expert's
+    bias changes nothing in either mode (softmax and the ordering are shift
+    invariant)."""
+    x = _rand((30, 8), 81)
+    wg = _rand((8, 6), 82, 0.5)
+    b = _rand((6,), 83)
+    plain = oracle.route(x, wg, 2, gate="fp64")
+    zero = oracle.route(x, wg, 2, bias=np.zeros(6), gate="fp64", bias_mode="select")
+    np.testing.assert_array_equal(zero["topk_idx"], plain["topk_idx"])
+    np.testing.assert_allclose(zero["topk_w"], plain["topk_w"], rtol=1e-15)
+    for mode in ("select", "logits"):
+        a = oracle.route(x, wg, 2, bias=b, gate="fp64", bias_mode=mode)
+        c = oracle.route(x, wg, 2, bias=b + 0.25, gate="fp64", bias_mode=mode)
+        np.testing.assert_array_equal(a["topk_idx"], c["topk_idx"])
+        np.testing.assert_allclose(a["topk_w"], c["topk_w"], rtol=1e-12)
+
+
+def test_fp32_selection_only_scores_add_the_bias_in_fp32():
+    """With the fp32 gate, the choosing score is fl32(fl32 logit + b): equal
+    to the bias-in-logits mode's score, so both modes choose the same experts."""
+    x = f32_to_bf16_bits(_rand((50, 64), 91).astype(np.float32))
+    wg = _rand((64, 16), 92, 0.05).astype(np.float32)
+    b = _rand((16,), 93, 0.5).astype(np.float32)
+    a = oracle.route(x, wg, 4, bias=b, bias_mode="select", want_logits=True)
+    c = oracle.route(x, wg, 4, bias=b, bias_mode="logits", want_logits=True)
+    np.testing.assert_array_equal(a["topk_idx"], c["topk_idx"])
+    np.testing.assert_array_equal(a["logits"], c["logits"])
+
+
+def test_balance_quantity_is_one_for_uniform_routing():
+    """[P3] s4.2: f_i = P_i = 1/N gives N * sum f_i P_i = 1 (the page's own
+    example); the entropy of a uniform load is log2 N and the top-1
+    probability is 1/N."""
+    for N, k, T in [(4, 1, 8), (8, 2, 12), (16, 4, 20), (64, 2, 64)]:
+        probs = np.full((T, N), 1.0 / N)
+        idx = np.array([[(t * k + j) % N for j in range(k)] for t in range(T)], np.int32)
+        st = oracle.load_stats(probs, idx)
+        assert st["balance"] == pytest.approx(GOLD["balance_loss_uniform"]["value"], rel=1e-14)
+        assert st["entropy_bits"] == pytest.approx(math.log2(N), rel=1e-14)
+        assert st["top1"] == pytest.approx(1.0 / N, rel=1e-14)
+        np.testing.assert_allclose(st["f"], 1.0 / N, rtol=1e-14)
+
+
+def test_activation_entropy_maximum_on_the_page():
+    """The page's 16-expert model has a maximum activation entropy of 4.0."""
+    g = GOLD["activation_entropy"]
+    N = g["experts"]
+    probs = np.full((N, N), 1.0 / N)
+    idx = np.arange(N, dtype=np.int32).reshape(N, 1)
+    assert oracle.load_stats(probs, idx)["entropy_bits"] == pytest.approx(g["max_bits"], abs=1e-14)
+
+
+def test_balance_quantity_collapse():
+    """Every token to expert 0 with probability 1: f_0 = P_0 = 1, so the
+    quantity is N; the entropy is 0 and the top-1 probability 1."""
+    N, T = 8, 10
+    probs = np.zeros((T, N))
+    probs[:, 0] = 1.0
+    st = oracle.load_stats(probs, np.zeros((T, 1), np.int32))
+    assert st["balance"] == N and st["entropy_bits"] == 0.0 and st["top1"] == 1.0
+
+
+def test_load_stats_against_library_routines():
+    """f = bincount / (T k), P = column mean of the softmax (scipy), top1 =
+    row max; sum f = sum P = 1; 0 <= entropy <= log2 N."""
+    T, d, N, k = 200, 16, 12, 3
+    x = _rand((T, d), 101)
+    wg = _rand((d, N), 102, 0.4)
+    r = oracle.route(x, wg, k, gate="fp64", want_probs=True)
+    st = oracle.load_stats(r["probs"], r["topk_idx"])
+    f = np.bincount(r["topk_idx"].ravel(), minlength=N) / (T * k)
+    p = special.softmax(x @ wg, axis=1)
+    np.testing.assert_allclose(st["f"], f, rtol=1e-14)
+    np.testing.assert_allclose(st["P"], p.mean(0), rtol=1e-12)
+    assert st["top1"] == pytest.approx(p.max(1).mean(), rel=1e-12)
+    assert st["f"].sum() == pytest.approx(1.0, rel=1e-14) and st["P"].sum() == pytest.approx(1.0, rel=1e-12)
+    assert 0.0 <= st["entropy_bits"] <= math.log2(N)
+    assert st["entropy_bits"] == pytest.approx(-(f[f > 0] * np.log2(f[f > 0])).sum(), rel=1e-13)
+
+
+def test_load_stats_empty_batch():
+    st = oracle.load_stats(np.zeros((0, 5)), np.zeros((0, 2), np.int32))
+    assert st["balance"] == 0.0 and st["entropy_bits"] == 0.0 and st["top1"] == 0.0

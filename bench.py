@@ -55,22 +55,39 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:12]
 
 
+GROUPED_GEMM_SOURCES = ("common.cuh", "schedule.cuh", "ffn_tc.cuh", "ffn_tc_swap.cuh")
+
+
+def grouped_gemm_source_hash() -> str:
+    """Hash of the sources the grouped-GEMM kernels are compiled from."""
+    h = hashlib.sha1()
+    cs = os.path.join(ROOT, "mixture_experts_layer_97_b300", "csrc")
+    for name in GROUPED_GEMM_SOURCES:
+        with open(os.path.join(cs, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the grouped GEMM from a committed ncu capture,
-    valid only while the kernel sources are unchanged since the capture."""
+    """DRAM bytes per moe_grouped_ffn call (both GEMM launches) from a
+    committed ncu capture, valid only while the grouped-GEMM sources are
+    unchanged since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             rec = json.load(f).get(workload)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != grouped_gemm_source_hash():
         return None
     return rec.get("bytes_per_call")
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons. The
+    sampler is started, and its first sample awaited, before the timed region;
+    summary() keeps the samples taken between mark_start() and mark_end()
+    (plus the one right after, which covers the region's last interval)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -78,22 +95,33 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []          # (monotonic time, csv line)
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.monotonic() + 5.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
+        time.sleep(0.12)         # let the sample that covers the region's end arrive
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -106,7 +134,13 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0 = self.t0 if self.t0 is not None else float("-inf")
+        t1 = self.t1 if self.t1 is not None else float("inf")
+        after = [ts for ts, _ in self.lines if ts > t1]
+        t1 = min(after) if after else t1      # include the first sample after the region
+        for ts, ln in self.lines:
+            if ts < t0 or ts > t1:
+                continue
             p = [c.strip() for c in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -321,10 +355,12 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.mark_start()
         for i in range(args.steps):
             flush.zero_()                      # L2 flush between timed steps (outside the events)
             step(evs[i])
         torch.cuda.synchronize()
+        clk.mark_end()
     if dist:
         dist.barrier()
     st = B.get_error()

@@ -79,6 +79,34 @@ moe_status moe_route(const moe_shape *s, const void *x, const float *w_g, const 
                      int32_t *topk_idx, float *topk_w, void *stream);
 
 /*
+ * Routing with a choice of bias mode and optional routing statistics.
+ * bias_mode MOE_BIAS_LOGITS: as moe_route (bias added to the logits before
+ * the softmax). MOE_BIAS_SELECT: the auxiliary-loss-free balancing of
+ * "MoE混合专家模型计算原理与推理部署实战解析" section 4.4 -- the experts are
+ * chosen by s = logit + bias (fp32 sum) but topk_w is the renormalised softmax
+ * of the logits WITHOUT the bias.
+ * load_stats (device, MOE_LOAD_STATS_LEN(N) floats, or NULL) receives, with p
+ * the softmax that weights the experts (over all N):
+ *   [0, N)     f[n] = assignments to expert n / (T*k)
+ *   [N, 2N)    P[n] = mean over tokens of p[t,n]
+ *   [2N]       N * sum_n f[n] * P[n]   (section 4.2 of the same page: 1 for
+ *              a uniform load, up to N when one expert takes everything)
+ *   [2N+1]     -sum_{f>0} f log2 f, the activation entropy in bits (maximum
+ *              log2 N; "这不是“参数越多越强”的简单故事" sections 3.1, 4.4)
+ *   [2N+2]     mean over tokens of max_n p[t,n] (top-1 confidence, same page
+ *              section 4.4)
+ * all zero for T = 0. Statistics are reduced in a fixed order (reproducible
+ * bit for bit). ws: moe_route_ex_workspace_size(s) bytes (may be NULL when
+ * load_stats is NULL). Other arguments as moe_route.
+ */
+typedef enum { MOE_BIAS_LOGITS = 0, MOE_BIAS_SELECT = 1 } moe_bias_mode;
+#define MOE_LOAD_STATS_LEN(N) (2 * (N) + 3)
+moe_status moe_route_ex(const moe_shape *s, const void *x, const float *w_g, const float *bias,
+                        int32_t bias_mode, int32_t *topk_idx, float *topk_w, float *load_stats,
+                        void *ws, size_t ws_bytes, void *stream);
+size_t moe_route_ex_workspace_size(const moe_shape *s);
+
+/*
  * Grouping by expert: "MoE显存与计算开销四阶段手算指南" section 2.3,
  * "MoE混合专家模型计算原理与推理部署实战解析" section 5.1 steps 2-3.
  *   counts[n]  = number of assignments to expert n (sum = T*k)
@@ -159,6 +187,28 @@ moe_status moe_forward_capacity(const moe_shape *s, double capacity_factor, cons
                                 const void *w_up, const void *w_down, void *out, int32_t *topk_idx,
                                 float *topk_w, int32_t *counts, int32_t *dropped, void *ws,
                                 size_t ws_bytes, void *stream);
+
+/*
+ * moe_forward with options, all optional and combinable:
+ *   bias_mode       moe_bias_mode (see moe_route_ex)
+ *   use_capacity    nonzero: expert capacity ceil(capacity_factor * T*k / N)
+ *                   as moe_permute_capacity (capacity_factor >= 0)
+ *   load_stats      device, MOE_LOAD_STATS_LEN(N) floats, or NULL (see
+ *                   moe_route_ex; statistics of the routing, before any drop)
+ *   dropped         device int32, or NULL: assignments dropped by the capacity
+ * opt == NULL is the plain moe_forward. ws: moe_workspace_size(s) bytes.
+ */
+typedef struct {
+    int32_t bias_mode;
+    int32_t use_capacity;
+    double capacity_factor;
+    float *load_stats;
+    int32_t *dropped;
+} moe_options;
+moe_status moe_forward_ex(const moe_shape *s, const moe_options *opt, const void *x, const float *w_g,
+                          const float *bias, const void *w_gate, const void *w_up,
+                          const void *w_down, void *out, int32_t *topk_idx, float *topk_w,
+                          int32_t *counts, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * moe_forward with x and out in HOST memory (pinned memory makes the copies

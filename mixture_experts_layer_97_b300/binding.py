@@ -34,7 +34,18 @@ class MoeShape(ctypes.Structure):
                 ("d_ff", ctypes.c_int32), ("act", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
+class MoeOptions(ctypes.Structure):
+    _fields_ = [("bias_mode", ctypes.c_int32), ("use_capacity", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
+                ("load_stats", ctypes.c_void_p), ("dropped", ctypes.c_void_p)]
+
+
 SP = ctypes.POINTER(MoeShape)
+OP = ctypes.POINTER(MoeOptions)
+BIAS_MODES = {"logits": 0, "select": 1}
+
+
+def load_stats_len(N: int) -> int:
+    return 2 * N + 3
 SIGNATURES = {
     "moe_route": (I32, [SP, P, P, P, P, P, P]),
     "moe_permute": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
@@ -42,6 +53,9 @@ SIGNATURES = {
     "moe_permute_noalloc": (I32, [SP, P, P, P, P, P, P, P, P]),
     "moe_permute_capacity": (I32, [SP, P, P, ctypes.c_double, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_capacity": (I32, [SP, ctypes.c_double, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_route_ex": (I32, [SP, P, P, P, I32, P, P, P, P, SZ, P]),
+    "moe_route_ex_workspace_size": (SZ, [SP]),
+    "moe_forward_ex": (I32, [SP, OP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_combine": (I32, [SP, P, P, P, P, P]),
     "moe_forward": (I32, [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_hostio": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
@@ -160,6 +174,34 @@ def permute_noalloc(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, str
     _check(lib().moe_permute_noalloc(ctypes.byref(s), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
                                      _ptr(perm), _ptr(inv_perm), _ptr(x_perm), _stream(stream)),
            "moe_permute_noalloc")
+
+
+def route_ex_workspace_size(s) -> int:
+    return lib().moe_route_ex_workspace_size(ctypes.byref(s))
+
+
+def route_ex(s, x, w_g, bias, topk_idx, topk_w, bias_mode="logits", load_stats=None, ws=None, stream=None):
+    _check(lib().moe_route_ex(ctypes.byref(s), _ptr(x), _ptr(w_g), _ptr(bias), BIAS_MODES[bias_mode], _ptr(topk_idx),
+                              _ptr(topk_w), _ptr(load_stats), _ptr(ws), ws.numel() if ws is not None else 0,
+                              _stream(stream)), "moe_route_ex")
+
+
+def unpack_load_stats(t, N: int) -> dict:
+    """The load_stats vector as named fields (host copy)."""
+    v = t.detach().cpu().numpy().astype("float64")
+    return dict(f=v[:N], P=v[N:2 * N], balance=float(v[2 * N]), entropy_bits=float(v[2 * N + 1]),
+                top1=float(v[2 * N + 2]))
+
+
+def forward_ex(s, x, w_g, bias, w_gate, w_up, w_down, out, ws, bias_mode="logits", capacity_factor=None,
+               load_stats=None, dropped=None, topk_idx=None, topk_w=None, counts=None, stream=None):
+    o = MoeOptions(BIAS_MODES[bias_mode], 0 if capacity_factor is None else 1,
+                   0.0 if capacity_factor is None else float(capacity_factor),
+                   None if load_stats is None else _ptr(load_stats).value,
+                   None if dropped is None else _ptr(dropped).value)
+    _check(lib().moe_forward_ex(ctypes.byref(s), ctypes.byref(o), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(w_gate),
+                                _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
+                                _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_ex")
 
 
 def permute_capacity(s, topk_idx, x, capacity_factor, counts, offsets, perm, inv_perm, x_perm, ws, dropped=None,

@@ -56,6 +56,20 @@ int64_t perm_chunks(const moe_shape* s) {
 
 size_t permute_ws(const moe_shape* s) { return align_up(sizeof(int32_t) * perm_chunks(s) * s->N); }
 size_t ffn_ws(const moe_shape* s) { return align_up(esize(s) * static_cast<size_t>(n_assign(s)) * s->d_ff); }
+// Statistics rows of one route launch: at most one per 4 tokens, 2N + 1 floats each.
+size_t route_stats_ws(const moe_shape* s) {
+  return align_up(sizeof(float) * static_cast<size_t>((s->T + 3) / 4) * (2 * static_cast<size_t>(s->N) + 1));
+}
+
+constexpr long long kNoCapacity = 0x7fffffffffffffffLL;
+
+// Options of one forward beyond the plain layer.
+struct FwdOpts {
+  int bias_select = 0;                 // the expert bias only chooses
+  long long capacity = kNoCapacity;    // rows an expert keeps
+  int32_t* dropped = nullptr;          // device [1]: dropped assignments
+  float* load_stats = nullptr;         // device [2N + 3]: routing statistics
+};
 
 struct FwdBufs {
   int32_t* topk_idx;
@@ -68,6 +82,7 @@ struct FwdBufs {
   void* y_perm;
   void* perm_ws;
   void* ffn_ws;
+  void* stats_ws;
   void* x_dev;     // hostio only
   void* out_dev;   // hostio only
   size_t total;
@@ -88,6 +103,7 @@ FwdBufs carve_forward(const moe_shape* s, void* ws, bool hostio) {
   b.y_perm = c.take<uint8_t>(es * A * s->d);
   b.perm_ws = c.take<uint8_t>(permute_ws(s));
   b.ffn_ws = c.take<uint8_t>(ffn_ws(s));
+  b.stats_ws = c.take<uint8_t>(route_stats_ws(s));
   if (hostio) {
     b.x_dev = c.take<uint8_t>(es * static_cast<size_t>(s->T) * s->d);
     b.out_dev = c.take<uint8_t>(es * static_cast<size_t>(s->T) * s->d);
@@ -133,9 +149,20 @@ int num_sms() {
 moe_status launched() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // ---------------------------------------------------------------- route
+// What one route launch writes besides the top-k; `rows` returns the number
+// of per-CTA statistics rows the launch produced.
+struct RouteArgs {
+  const float* wg;
+  const float* bias;
+  int bias_select;
+  int32_t* idx;
+  float* w;
+  float* stats_part;   // [grid][2N + 1] or null
+  int64_t rows;
+};
+
 template <int EG, int EPT, int TPT, typename TX>
-moe_status launch_route_cfg(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx,
-                            float* w, cudaStream_t st) {
+moe_status launch_route_cfg(const moe_shape* s, const TX* x, RouteArgs& a, cudaStream_t st) {
   using Cfg = RouteCfg<EG, EPT, TPT, TX>;
   auto kern = route_kernel<EG, EPT, TPT, TX>;
   if (Cfg::kSmem > 48 * 1024 &&
@@ -143,28 +170,28 @@ moe_status launch_route_cfg(const moe_shape* s, const TX* x, const float* wg, co
           cudaSuccess)
     return MOE_ERR_CUDA;
   const int64_t grid = (s->T + Cfg::TM - 1) / Cfg::TM;
-  kern<<<static_cast<unsigned>(grid), kRouteThreads, Cfg::kSmem, st>>>(x, wg, bias, static_cast<int>(s->T), s->d,
-                                                                        s->N, s->k, idx, w);
+  a.rows = grid;
+  kern<<<static_cast<unsigned>(grid), kRouteThreads, Cfg::kSmem, st>>>(
+      x, a.wg, a.bias, static_cast<int>(s->T), s->d, s->N, s->k, a.bias_select, a.idx, a.w, a.stats_part);
   return launched();
 }
 
 // Experts padded to NP = EG * EPT, the smallest power of two >= max(N, EG);
 // tokens per CTA TM = (256 / EG) * TPT.
 template <int EG, int TPT, typename TX>
-moe_status launch_route_tm(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx,
-                           float* w, cudaStream_t st) {
-  if (s->N <= EG) return launch_route_cfg<EG, 1, TPT, TX>(s, x, wg, bias, idx, w, st);
+moe_status launch_route_tm(const moe_shape* s, const TX* x, RouteArgs& a, cudaStream_t st) {
+  if (s->N <= EG) return launch_route_cfg<EG, 1, TPT, TX>(s, x, a, st);
   if constexpr (EG * 2 <= 256) {
-    if (s->N <= EG * 2) return launch_route_cfg<EG, 2, TPT, TX>(s, x, wg, bias, idx, w, st);
+    if (s->N <= EG * 2) return launch_route_cfg<EG, 2, TPT, TX>(s, x, a, st);
   }
   if constexpr (EG * 4 <= 256) {
-    if (s->N <= EG * 4) return launch_route_cfg<EG, 4, TPT, TX>(s, x, wg, bias, idx, w, st);
+    if (s->N <= EG * 4) return launch_route_cfg<EG, 4, TPT, TX>(s, x, a, st);
   }
   if constexpr (EG * 8 <= 256) {
-    if (s->N <= EG * 8) return launch_route_cfg<EG, 8, TPT, TX>(s, x, wg, bias, idx, w, st);
+    if (s->N <= EG * 8) return launch_route_cfg<EG, 8, TPT, TX>(s, x, a, st);
   }
   if constexpr (EG * 16 <= 256) {
-    if (s->N <= EG * 16) return launch_route_cfg<EG, 16, TPT, TX>(s, x, wg, bias, idx, w, st);
+    if (s->N <= EG * 16) return launch_route_cfg<EG, 16, TPT, TX>(s, x, a, st);
   }
   return MOE_ERR_UNSUPPORTED;
 }
@@ -173,31 +200,36 @@ moe_status launch_route_tm(const moe_shape* s, const TX* x, const float* wg, con
 // from tokens x experts: pick the largest token tile that still gives every
 // SM a CTA, down to 4 tokens per CTA for decode-sized batches.
 template <typename TX>
-moe_status launch_route(const moe_shape* s, const TX* x, const float* wg, const float* bias, int32_t* idx, float* w,
-                        cudaStream_t st) {
+moe_status launch_route(const moe_shape* s, const TX* x, RouteArgs& a, cudaStream_t st) {
+  a.rows = 0;
   if (s->T == 0) return MOE_OK;
   const int64_t sms = num_sms();
   const int64_t T = s->T;
   if (s->N <= 8) {   // 8 expert lanes: few experts are not padded to 16 or 32
-    if ((T + 127) / 128 >= sms) return launch_route_tm<8, 4, TX>(s, x, wg, bias, idx, w, st);   // 128 tokens/CTA
-    if ((T + 63) / 64 >= sms) return launch_route_tm<8, 2, TX>(s, x, wg, bias, idx, w, st);     // 64 tokens/CTA
-    return launch_route_tm<8, 1, TX>(s, x, wg, bias, idx, w, st);                                // 32 tokens/CTA
+    if ((T + 127) / 128 >= sms) return launch_route_tm<8, 4, TX>(s, x, a, st);   // 128 tokens/CTA
+    if ((T + 63) / 64 >= sms) return launch_route_tm<8, 2, TX>(s, x, a, st);     // 64 tokens/CTA
+    return launch_route_tm<8, 1, TX>(s, x, a, st);                                // 32 tokens/CTA
   }
-  if ((T + 63) / 64 >= sms) return launch_route_tm<16, 4, TX>(s, x, wg, bias, idx, w, st);       // 64 tokens/CTA
-  if ((T + 31) / 32 >= sms) return launch_route_tm<16, 2, TX>(s, x, wg, bias, idx, w, st);       // 32 tokens/CTA
-  if ((T + 7) / 8 >= sms / 2) return launch_route_tm<32, 1, TX>(s, x, wg, bias, idx, w, st);     // 8 tokens/CTA
-  return launch_route_tm<64, 1, TX>(s, x, wg, bias, idx, w, st);                                 // 4 tokens/CTA
+  if ((T + 63) / 64 >= sms) return launch_route_tm<16, 4, TX>(s, x, a, st);       // 64 tokens/CTA
+  if ((T + 31) / 32 >= sms) return launch_route_tm<16, 2, TX>(s, x, a, st);       // 32 tokens/CTA
+  if ((T + 7) / 8 >= sms / 2) return launch_route_tm<32, 1, TX>(s, x, a, st);     // 8 tokens/CTA
+  return launch_route_tm<64, 1, TX>(s, x, a, st);                                 // 4 tokens/CTA
 }
 
+// Route, then (when load_stats is given) reduce the statistics rows that the
+// route kernel left in stats_ws.
 moe_status route_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, int32_t* idx, float* w,
-                      cudaStream_t st) {
-  if (s->dtype == MOE_BF16)
-    return launch_route<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(x), wg, bias, idx, w, st);
-  return launch_route<float>(s, static_cast<const float*>(x), wg, bias, idx, w, st);
+                      cudaStream_t st, int bias_select = 0, float* load_stats = nullptr, void* stats_ws = nullptr) {
+  RouteArgs a{wg, bias, bias_select, idx, w, load_stats ? static_cast<float*>(stats_ws) : nullptr, 0};
+  moe_status r = s->dtype == MOE_BF16
+                     ? launch_route<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(x), a, st)
+                     : launch_route<float>(s, static_cast<const float*>(x), a, st);
+  if (r != MOE_OK || load_stats == nullptr) return r;
+  route_stats_kernel<<<1, 256, 0, st>>>(a.stats_part, a.rows, s->T, s->N, s->k, load_stats);
+  return launched();
 }
 
 // ---------------------------------------------------------------- permute
-constexpr long long kNoCapacity = 0x7fffffffffffffffLL;
 
 moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, int32_t* counts, int32_t* offsets,
                         int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, cudaStream_t st,
@@ -403,14 +435,13 @@ moe_status combine_impl(const moe_shape* s, const void* y_perm, const int32_t* i
 
 moe_status forward_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, const void* w_gate,
                         const void* w_up, const void* w_down, void* out, int32_t* topk_idx, float* topk_w,
-                        int32_t* counts, const FwdBufs& b, cudaStream_t st, long long capacity = kNoCapacity,
-                        int32_t* dropped = nullptr) {
+                        int32_t* counts, const FwdBufs& b, cudaStream_t st, const FwdOpts& o = FwdOpts{}) {
   int32_t* idx = topk_idx ? topk_idx : b.topk_idx;
   float* w = topk_w ? topk_w : b.topk_w;
   int32_t* cnt = counts ? counts : b.counts;
-  moe_status r = route_impl(s, x, wg, bias, idx, w, st);
+  moe_status r = route_impl(s, x, wg, bias, idx, w, st, o.bias_select, o.load_stats, b.stats_ws);
   if (r != MOE_OK) return r;
-  r = permute_impl(s, idx, x, cnt, b.offsets, b.perm, b.inv_perm, b.x_perm, b.perm_ws, st, capacity, dropped);
+  r = permute_impl(s, idx, x, cnt, b.offsets, b.perm, b.inv_perm, b.x_perm, b.perm_ws, st, o.capacity, o.dropped);
   if (r != MOE_OK) return r;
   r = ffn_impl(s, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st);
   if (r != MOE_OK) return r;
@@ -463,6 +494,24 @@ moe_status moe_route(const moe_shape* s, const void* x, const float* w_g, const 
       !ptr_ok(topk_w, any))
     return MOE_ERR_INVALID_ARG;
   return route_impl(s, x, w_g, bias, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_route_ex_workspace_size(const moe_shape* s) { return shape_status(s) == MOE_OK ? route_stats_ws(s) : 0; }
+
+moe_status moe_route_ex(const moe_shape* s, const void* x, const float* w_g, const float* bias, int32_t bias_mode,
+                        int32_t* topk_idx, float* topk_w, float* load_stats, void* ws, size_t ws_bytes,
+                        void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  if (bias_mode != MOE_BIAS_LOGITS && bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
+  const bool any = s->T > 0;
+  const bool stats = load_stats != nullptr;
+  if (!ptr_ok(x, any) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) || !ptr_ok(topk_idx, any) ||
+      !ptr_ok(topk_w, any) || !ptr_ok(load_stats, false) || !ptr_ok(ws, stats && any))
+    return MOE_ERR_INVALID_ARG;
+  if (stats && ws_bytes < route_stats_ws(s)) return MOE_ERR_WORKSPACE;
+  return route_impl(s, x, w_g, bias, topk_idx, topk_w, static_cast<cudaStream_t>(stream),
+                    bias_mode == MOE_BIAS_SELECT ? 1 : 0, load_stats, ws);
 }
 
 moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const void* x, int32_t* counts,
@@ -547,8 +596,38 @@ moe_status moe_forward_capacity(const moe_shape* s, double capacity_factor, cons
     return MOE_ERR_INVALID_ARG;
   const FwdBufs b = carve_forward(s, ws, false);
   if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  FwdOpts o;
+  o.capacity = capacity_rows(s, capacity_factor);
+  o.dropped = dropped;
   return forward_impl(s, x, w_g, bias, w_gate, w_up, w_down, out, topk_idx, topk_w, counts, b,
-                      static_cast<cudaStream_t>(stream), capacity_rows(s, capacity_factor), dropped);
+                      static_cast<cudaStream_t>(stream), o);
+}
+
+moe_status moe_forward_ex(const moe_shape* s, const moe_options* opt, const void* x, const float* w_g,
+                          const float* bias, const void* w_gate, const void* w_up, const void* w_down, void* out,
+                          int32_t* topk_idx, float* topk_w, int32_t* counts, void* ws, size_t ws_bytes,
+                          void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  FwdOpts o;
+  if (opt != nullptr) {
+    if (opt->bias_mode != MOE_BIAS_LOGITS && opt->bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
+    if (opt->use_capacity && !(opt->capacity_factor >= 0.0)) return MOE_ERR_INVALID_ARG;
+    if (!ptr_ok(opt->load_stats, false) || !ptr_ok(opt->dropped, false)) return MOE_ERR_INVALID_ARG;
+    o.bias_select = opt->bias_mode == MOE_BIAS_SELECT ? 1 : 0;
+    if (opt->use_capacity) o.capacity = capacity_rows(s, opt->capacity_factor);
+    o.load_stats = opt->load_stats;
+    o.dropped = opt->dropped;
+  }
+  const bool any = s->T > 0;
+  if (!ptr_ok(x, any) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) || !weights_ok(s, w_gate, w_up, w_down) ||
+      !ptr_ok(out, any) || !ptr_ok(topk_idx, false) || !ptr_ok(topk_w, false) || !ptr_ok(counts, false) ||
+      !ptr_ok(ws, true))
+    return MOE_ERR_INVALID_ARG;
+  const FwdBufs b = carve_forward(s, ws, false);
+  if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  return forward_impl(s, x, w_g, bias, w_gate, w_up, w_down, out, topk_idx, topk_w, counts, b,
+                      static_cast<cudaStream_t>(stream), o);
 }
 
 moe_status moe_forward_hostio(const moe_shape* s, const void* x_host, const float* w_g, const float* bias,

@@ -9,6 +9,22 @@
 // evaluates w_j = exp(s_j - s_max) / sum_j' exp(s_j' - s_max) over the k
 // selected scores only (identical in exact arithmetic).
 //
+// Expert bias, two modes: added to the logits before the softmax (so it moves
+// both the choice and the weights), or -- the auxiliary-loss-free balancing
+// of "MoE混合专家模型计算原理与推理部署实战解析" section 4.4 -- added only to the
+// scores that choose the experts, the weights then coming from the softmax of
+// the unbiased logits. Either way the choosing score is the fp32 sum
+// logit + b.
+//
+// Routing statistics (optional): each CTA writes, for its tokens, the sum of
+// the full softmax p[t,n] per expert, the number of assignments per expert,
+// and the sum of the top-1 probabilities, in a fixed order;
+// route_stats_kernel reduces the per-CTA rows into the load statistics of
+// section 4.2 of the same page (fraction routed f, mean probability P,
+// N * sum f P) plus the activation entropy and mean top-1 probability of
+// "这不是“参数越多越强”的简单故事" sections 3.1 and 4.4. No float atomics: the
+// statistics are reproducible bit for bit.
+//
 // Each logit is the sequential FMA chain over i = 0..d-1 in index order (one
 // thread owns it from start to end), then one fp32 bias add: the plainest fp32
 // evaluation, so the top-k decision is reproducible bit for bit.
@@ -39,7 +55,9 @@ struct RouteCfg {
   static constexpr int WBYTES = kRouteBK * NP * 4;                           // one stage of W_g
   static constexpr size_t kPipe = static_cast<size_t>(STAGES) * (XBYTES + WBYTES);
   static constexpr size_t kLogits = sizeof(float) * TM * (NP + 1);
-  static constexpr size_t kSmem = kPipe > kLogits ? kPipe : kLogits;
+  // per-warp statistics rows [8][2*NP + 1] after the logit tile
+  static constexpr size_t kStats = kLogits + sizeof(float) * (kRouteThreads / 32) * (2 * NP + 1);
+  static constexpr size_t kSmem = kPipe > kStats ? kPipe : kStats;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -69,8 +87,10 @@ __device__ __forceinline__ void load_x8(const float* p, float* v) {
 template <int EG, int EPT, int TPT, typename TX>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restrict__ x, const float* __restrict__ wg,
                                                               const float* __restrict__ bias, int T, int d, int N,
-                                                              int k, int32_t* __restrict__ topk_idx,
-                                                              float* __restrict__ topk_w) {
+                                                              int k, int bias_select,
+                                                              int32_t* __restrict__ topk_idx,
+                                                              float* __restrict__ topk_w,
+                                                              float* __restrict__ stats_part) {
   using C = RouteCfg<EG, EPT, TPT, TX>;
   constexpr int NP = C::NP, TM = C::TM, S = C::STAGES;
   constexpr int NPR = NP < 32 ? 32 : NP;   // register slots per token for the argmax
@@ -175,11 +195,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
   cp_async_wait<0>();
   __syncthreads();
 
-  // logits (+ bias) -> lg[token][n]; padded experts get -inf
+  // logits (+ bias, unless it only chooses) -> lg[token][n]; padded experts get -inf
 #pragma unroll
   for (int j = 0; j < EPT; ++j) {
     const int n = V * tx + V * EG * (j / V) + (j % V);
-    const float b = (bias != nullptr && n < N) ? bias[n] : 0.f;
+    const float b = (bias != nullptr && !bias_select && n < N) ? bias[n] : 0.f;
 #pragma unroll
     for (int i = 0; i < TPT; ++i) lg[(ty * TPT + i) * (NP + 1) + n] = (n < N) ? acc[i][j] + b : -INFINITY;
   }
@@ -187,15 +207,29 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
 
   // top-k: one warp per token, k rounds of warp argmax (ties -> lower id)
   const int warp = tid >> 5, lane = tid & 31;
+  const bool want_stats = stats_part != nullptr;
+  float bsel[SLOTS];          // the bias of the choosing score when it only chooses
+  float p_acc[SLOTS];         // statistics: sum over this warp's tokens of p[t,n]
+  float c_acc[SLOTS];         //             assignments to n
+  float top1_acc = 0.f;       //             sum of the top-1 probabilities
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const int n = lane + 32 * m;
+    bsel[m] = (bias != nullptr && bias_select && n < N) ? bias[n] : 0.f;
+    p_acc[m] = 0.f;
+    c_acc[m] = 0.f;
+  }
   for (int tl = warp; tl < TM; tl += kRouteThreads / 32) {
     const int64_t t = t0 + tl;
     if (t >= T) break;
-    float v[SLOTS];
+    float g[SLOTS];           // logits of the softmax
+    float v[SLOTS];           // choosing scores
     bool taken[SLOTS];
 #pragma unroll
     for (int m = 0; m < SLOTS; ++m) {
       const int n = lane + 32 * m;
-      v[m] = (n < NP) ? lg[tl * (NP + 1) + n] : -INFINITY;
+      g[m] = (n < NP) ? lg[tl * (NP + 1) + n] : -INFINITY;
+      v[m] = (n < N) ? g[m] + bsel[m] : -INFINITY;
       taken[m] = (n >= N);
     }
     float sel_v[SLOTS];
@@ -217,12 +251,40 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
         const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
         if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
       }
-      if (j == 0) top = bv;
+      // the winner's softmax logit (its score unless the bias only chooses)
+      float gw = -INFINITY;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m)
+        if ((bi >> 5) == m) gw = g[m];
+      gw = __shfl_sync(0xffffffffu, gw, bi & 31);
+      top = (j == 0) ? gw : fmaxf(top, gw);
 #pragma unroll
       for (int m = 0; m < SLOTS; ++m) {
-        if (bi == lane + 32 * m) taken[m] = true;
-        if ((j & 31) == lane && (j >> 5) == m) { sel_v[m] = bv; sel_i[m] = bi; }
+        if (bi == lane + 32 * m) {
+          taken[m] = true;
+          c_acc[m] += 1.f;
+        }
+        if ((j & 31) == lane && (j >> 5) == m) { sel_v[m] = gw; sel_i[m] = bi; }
       }
+    }
+    if (want_stats) {         // full softmax over the N experts
+      float gmax = -INFINITY;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) gmax = fmaxf(gmax, g[m]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+      float e[SLOTS], z = 0.f;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) {
+        e[m] = (lane + 32 * m < N) ? expf(g[m] - gmax) : 0.f;
+        z += e[m];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      const float iz = 1.f / z;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) p_acc[m] += e[m] * iz;
+      top1_acc += iz;         // p of the largest logit is exp(0) / z
     }
     float part = 0.f;
     float ex[SLOTS];
@@ -243,6 +305,83 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
         topk_w[t * k + j] = ex[m] * inv;
       }
     }
+  }
+  if (!want_stats) return;
+  // per-warp rows -> one row per CTA: [N probability sums | N counts | top-1 sum]
+  float* srow = reinterpret_cast<float*>(route_smem + C::kLogits);   // [8][2*NP + 1]
+  constexpr int SW = 2 * NP + 1;
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const int n = lane + 32 * m;
+    if (n < NP) {
+      srow[warp * SW + n] = p_acc[m];
+      srow[warp * SW + NP + n] = c_acc[m];
+    }
+  }
+  if (lane == 0) srow[warp * SW + 2 * NP] = top1_acc;
+  __syncthreads();
+  float* out = stats_part + static_cast<int64_t>(blockIdx.x) * (2 * N + 1);
+  for (int n = tid; n < N; n += kRouteThreads) {
+    float ps = 0.f, cs = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRouteThreads / 32; ++w) {
+      ps += srow[w * SW + n];
+      cs += srow[w * SW + NP + n];
+    }
+    out[n] = ps;
+    out[N + n] = cs;
+  }
+  if (tid == 0) {
+    float ts = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRouteThreads / 32; ++w) ts += srow[w * SW + 2 * NP];
+    out[2 * N] = ts;
+  }
+}
+
+// Load statistics from the route kernel's per-CTA rows (one CTA, 256 threads,
+// thread n owns expert n; sums in CTA order, in fp64). out layout:
+//   out[0, N)    f[n] = assignments to n / (T k)
+//   out[N, 2N)   P[n] = mean over tokens of p[t,n]
+//   out[2N]      N * sum_n f[n] P[n]        (1 for a uniform load)
+//   out[2N + 1]  -sum_{f > 0} f log2 f      (activation entropy, bits)
+//   out[2N + 2]  mean top-1 probability
+// An empty batch gives zeros.
+__global__ void __launch_bounds__(256) route_stats_kernel(const float* __restrict__ part, int64_t n_rows,
+                                                          int64_t T, int N, int k, float* __restrict__ out) {
+  __shared__ double red_b[256], red_e[256];
+  const int n = threadIdx.x;
+  const int64_t W = 2 * N + 1;
+  double bal = 0.0, ent = 0.0;
+  if (n < N) {
+    double ps = 0.0, cs = 0.0;
+    for (int64_t c = 0; c < n_rows; ++c) {
+      ps += part[c * W + n];
+      cs += part[c * W + N + n];
+    }
+    const double f = T > 0 ? cs / (static_cast<double>(T) * k) : 0.0;
+    const double P = T > 0 ? ps / static_cast<double>(T) : 0.0;
+    out[n] = static_cast<float>(f);
+    out[N + n] = static_cast<float>(P);
+    bal = f * P;
+    ent = f > 0.0 ? -f * log2(f) : 0.0;
+  }
+  red_b[n] = bal;
+  red_e[n] = ent;
+  __syncthreads();
+  for (int h = 128; h > 0; h >>= 1) {
+    if (n < h) {
+      red_b[n] += red_b[n + h];
+      red_e[n] += red_e[n + h];
+    }
+    __syncthreads();
+  }
+  if (n == 0) {
+    double ts = 0.0;
+    for (int64_t c = 0; c < n_rows; ++c) ts += part[c * W + 2 * N];
+    out[2 * N] = static_cast<float>(static_cast<double>(N) * red_b[0]);
+    out[2 * N + 1] = static_cast<float>(red_e[0]);
+    out[2 * N + 2] = T > 0 ? static_cast<float>(ts / static_cast<double>(T)) : 0.f;
   }
 }
 

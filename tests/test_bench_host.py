@@ -51,11 +51,15 @@ def test_single_rank_is_identity():
 
 def test_clock_summary_parses_and_flags_throttling():
     c = bench.ClockSampler(0)
-    c.lines = ["0, 1900, 2032, 900.0, 0x4, Not Active, Not Active, Not Active, Active",
-               "0, 2000, 2032, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
-               "0, 1950, 2032, 980.0, 0x0, Active, Not Active, Not Active, Not Active",
-               "garbage"]
+    c.lines = [(0.9, "0, 1000, 2032, 300.0, 0x0, Not Active, Not Active, Active, Not Active"),   # before the region
+               (1.1, "0, 1900, 2032, 900.0, 0x4, Not Active, Not Active, Not Active, Active"),
+               (1.2, "0, 2000, 2032, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active"),
+               (1.3, "0, 1950, 2032, 980.0, 0x0, Active, Not Active, Not Active, Not Active"),
+               (1.35, "garbage"),
+               (1.45, "0, 1960, 2032, 980.0, 0x0, Not Active, Not Active, Not Active, Not Active"),  # covers the end
+               (1.6, "0, 500, 2032, 100.0, 0x0, Not Active, Active, Not Active, Not Active")]      # after
+    c.t0, c.t1 = 1.0, 1.4
     r = c.summary()
-    assert r["sm_mhz"] == 1950 and r["sm_max_mhz"] == 2032 and r["samples"] == 3
+    assert r["sm_mhz"] == 1955 and r["sm_max_mhz"] == 2032 and r["samples"] == 4
     assert r["reasons"] == ["hw_slowdown", "sw_power_cap"]
     assert bench.ClockSampler(0).summary()["samples"] == 0

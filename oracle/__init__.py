@@ -65,6 +65,8 @@ def lib():
         L.oracle_expert_rows.restype = I
         L.oracle_combine.argtypes = [I64, P, I, I, P, P, P, P]
         L.oracle_combine.restype = I
+        L.oracle_expert_choice.argtypes = [I64, I, I64, P, P, P, P, P, P, P]
+        L.oracle_expert_choice.restype = I
         L.oracle_load_stats.argtypes = [I64, I, I, P, P, P, P, P]
         L.oracle_load_stats.restype = I
         L.oracle_forward.argtypes = [I64, I, I, I, I, I, P, I, P, I, P, I, I, I, P, P, P, I,
@@ -181,6 +183,27 @@ def permute_capacity(topk_idx, N, cap):
         raise ValueError("oracle_permute_capacity: expert index out of range")
     kept = int(offsets[N])
     return dict(counts=counts, offsets=offsets, perm=perm[:kept], inv_perm=inv, dropped=int(dropped))
+
+
+def expert_choice(probs, C):
+    """Expert-choice routing on the gate probabilities [T, N]: each expert
+    takes its C most probable tokens (equal -> lower token id). Returns
+    perm [N*C] (row -> token, expert e's rows e*C.. in ascending token
+    order), w_row [N*C], inv [T, N] (row or -2), w [T, N] (p or 0), and per
+    expert thr (smallest value picked) / next (largest value left, -1 when
+    C == T)."""
+    probs = np.ascontiguousarray(probs, dtype=np.float64)
+    T, N = probs.shape
+    C = int(C)
+    perm = np.empty(max(N * C, 1), np.int32)
+    w_row = np.empty(max(N * C, 1), np.float64)
+    inv = np.empty((T, N), np.int32)
+    w = np.empty((T, N), np.float64)
+    thr = np.empty(N, np.float64)
+    nxt = np.empty(N, np.float64)
+    if lib().oracle_expert_choice(T, N, C, _p(probs), _p(perm), _p(w_row), _p(inv), _p(w), _p(thr), _p(nxt)):
+        raise ValueError("oracle_expert_choice: bad arguments (need 0 <= C <= T)")
+    return dict(perm=perm[:N * C], w_row=w_row[:N * C], inv=inv, w=w, thr=thr, next=nxt)
 
 
 def expert_rows(x_rows, w_gate, w_up, w_down, act, want_h=False):

@@ -339,6 +339,63 @@ int oracle_load_stats(int64_t T, int N, int k, const double *probs, const int32_
     return 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * Expert-choice routing: [P3] s2.3 (each expert picks its own top tokens, so
+ * every expert processes exactly the same number and a token may be picked
+ * by no expert). Readings where the page is silent:
+ *   - the token-expert affinity is the gate probability p[t,e] = softmax over
+ *     the experts of token t's logits (probs of oracle_route), the quantity
+ *     the token-choice top-k of s2.1 ranks;
+ *   - expert e takes the C tokens of largest p[t,e]; equal values -> lower t;
+ *   - a picked token is weighted by p[t,e] itself (no renormalisation);
+ *   - expert e's rows are e*C .. e*C + C - 1, its tokens in ascending order.
+ * Outputs:
+ *   perm[e*C + i] = token of expert e's i-th row; w_row[same] = p[t,e]
+ *   inv[t*N + e] = row, or -2 when e did not pick t; w[t*N + e] = p[t,e] or 0
+ *   thr[e]  = the C-th largest p[.,e] (the smallest value picked)
+ *   next[e] = the (C+1)-th largest (the largest value left), -1 when C == T
+ * The combine is then oracle_combine with k = N over inv / w.
+ * Returns 0, or -1 on bad arguments (needs 0 <= C <= T).
+ * ------------------------------------------------------------------------- */
+typedef struct { double p; int64_t t; } ec_item;
+
+static int ec_cmp(const void *a, const void *b)
+{
+    const ec_item *x = (const ec_item *)a, *y = (const ec_item *)b;
+    if (x->p > y->p) return -1;
+    if (x->p < y->p) return 1;
+    return (x->t < y->t) ? -1 : (x->t > y->t);
+}
+
+int oracle_expert_choice(int64_t T, int N, int64_t C, const double *probs,
+                         int32_t *perm, double *w_row, int32_t *inv, double *w, double *thr, double *next)
+{
+    if (T < 0 || N < 1 || C < 0 || C > T) return -1;
+    for (int64_t i = 0; i < T * N; ++i) { inv[i] = -2; w[i] = 0.0; }
+    ec_item *it = (ec_item *)malloc(sizeof(ec_item) * (size_t)(T > 0 ? T : 1));
+    unsigned char *picked = (unsigned char *)malloc((size_t)(T > 0 ? T : 1));
+    if (!it || !picked) { free(it); free(picked); return -1; }
+    for (int e = 0; e < N; ++e) {
+        for (int64_t t = 0; t < T; ++t) { it[t].p = probs[t * N + e]; it[t].t = t; picked[t] = 0; }
+        qsort(it, (size_t)T, sizeof(ec_item), ec_cmp);
+        for (int64_t i = 0; i < C; ++i) picked[it[i].t] = 1;
+        thr[e] = C > 0 ? it[C - 1].p : INFINITY;
+        next[e] = C < T ? it[C].p : -1.0;
+        int64_t row = (int64_t)e * C;
+        for (int64_t t = 0; t < T; ++t) {
+            if (!picked[t]) continue;
+            perm[row] = (int32_t)t;
+            w_row[row] = probs[t * N + e];
+            inv[t * N + e] = (int32_t)row;
+            w[t * N + e] = probs[t * N + e];
+            ++row;
+        }
+    }
+    free(it);
+    free(picked);
+    return 0;
+}
+
 /* SiLU and tanh-GELU, [P3] s3.1 (SiLU(gate) * up). */
 static double silu(double v) { return v / (1.0 + exp(-v)); }
 static double gelu_tanh(double v)

@@ -582,3 +582,75 @@ def test_load_stats_against_library_routines():
 def test_load_stats_empty_batch():
     st = oracle.load_stats(np.zeros((0, 5)), np.zeros((0, 2), np.int32))
     assert st["balance"] == 0.0 and st["entropy_bits"] == 0.0 and st["top1"] == 0.0
+
+
+# ---------------------------------------------------------------- expert-choice routing
+def _probs(T, N, seed, scale=1.0):
+    return special.softmax(_rand((T, N), seed, scale), axis=1)
+
+
+@pytest.mark.parametrize("T,N,C", [(10, 3, 4), (50, 8, 13), (64, 5, 64), (7, 7, 0), (30, 4, 1)])
+def test_expert_choice_matches_lexsort(T, N, C):
+    """Each expert's tokens = the first C of a lexicographic sort by (p
+    descending, token ascending) -- numpy's lexsort as the independent
+    routine; rows list them in ascending token order; every expert gets
+    exactly C (the page's balanced load)."""
+    p = _probs(T, N, T + N)
+    r = oracle.expert_choice(p, C)
+    assert r["perm"].shape == (N * C,)
+    for e in range(N):
+        order = np.lexsort((np.arange(T), -p[:, e]))[:C]
+        rows = r["perm"][e * C:(e + 1) * C]
+        np.testing.assert_array_equal(rows, np.sort(order))
+        np.testing.assert_array_equal(r["w_row"][e * C:(e + 1) * C], p[rows, e])
+        if C:
+            assert r["thr"][e] == p[order[-1], e]
+        assert (r["inv"][:, e] >= 0).sum() == C
+    # inv / w are the inverse of perm / w_row
+    for row in range(N * C):
+        t, e = r["perm"][row], row // C
+        assert r["inv"][t, e] == row and r["w"][t, e] == p[t, e]
+    assert np.all((r["inv"] >= 0) | (r["inv"] == -2))
+    assert np.all(r["w"][r["inv"] == -2] == 0.0)
+
+
+def test_expert_choice_ties_take_the_lower_token():
+    p = np.array([[.5, .5], [.5, .5], [.9, .1], [.5, .5]])
+    r = oracle.expert_choice(p, 2)
+    assert r["perm"].tolist() == [0, 2, 0, 1]       # expert 0: .9 then the first .5; expert 1: tokens 0, 1
+
+
+def test_expert_choice_can_leave_a_token_unpicked():
+    """[P3] s2.3: a token may be picked by no expert."""
+    p = np.array([[.6, .4], [.7, .3], [.2, .8], [.5, .5]])
+    r = oracle.expert_choice(p, 1)
+    assert r["perm"].tolist() == [1, 2]
+    assert np.all(r["inv"][0] == -2) and np.all(r["inv"][3] == -2)
+    assert "2.3" in GOLD["expert_choice"]["_cite"]
+
+
+def test_expert_choice_all_tokens_with_identical_experts_is_the_dense_ffn():
+    """C = T: every expert takes every token; with N identical experts the
+    combine gives sum_e p[t,e] * FFN(x_t) = FFN(x_t), because the
+    probabilities of a token sum to 1 (the dense tanh-GELU FFN is written out
+    here with numpy)."""
+    T, d, N, F = 12, 16, 4, 24
+    x = _rand((T, d), 111)
+    wg = _rand((d, N), 112, 0.5)
+    W1 = _rand((F, d), 113, 0.3)
+    W2 = _rand((d, F), 114, 0.3)
+    r = oracle.route(x, wg, 1, gate="fp64", want_probs=True)
+    ec = oracle.expert_choice(r["probs"], T)
+    y = np.zeros((N * T, d))
+    for e in range(N):
+        rows = ec["perm"][e * T:(e + 1) * T]
+        y[e * T:(e + 1) * T] = oracle.expert_rows(x[rows], W1, None, W2, "gelu_tanh")
+    out = oracle.combine(y, ec["inv"], ec["w"])
+    hpre = x @ W1.T
+    dense = (0.5 * hpre * (1 + np.tanh(np.sqrt(2 / np.pi) * (hpre + 0.044715 * hpre ** 3)))) @ W2.T
+    np.testing.assert_allclose(out, dense, rtol=1e-12, atol=1e-12)
+
+
+def test_expert_choice_rejects_capacity_above_tokens():
+    with pytest.raises(ValueError):
+        oracle.expert_choice(_probs(4, 2, 1), 5)

@@ -261,7 +261,11 @@ def main():
                     help="tensor-core tiling of the grouped GEMMs (library default: auto)")
     ap.add_argument("--capacity-factor", type=float, default=None,
                     help="expert capacity ceil(cf * T * k / N); overflow assignments are dropped")
+    ap.add_argument("--routing", default="token", choices=["token", "expert"],
+                    help="token choice (top-k per token) or expert choice (each expert takes C = T*k/N tokens)")
     args = ap.parse_args()
+    if args.routing == "expert" and args.capacity_factor is not None:
+        ap.error("--capacity-factor applies to token-choice routing only")
     args.warmup = max(args.warmup, 3)
     w0 = S.WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -282,7 +286,7 @@ def main():
     w = replica_workload(w0, rank)
 
     # cpu sample plan first (host only), so its experts can be kept while uploading
-    do_cpu = rank == 0 and not args.no_cpu_baseline
+    do_cpu = rank == 0 and not args.no_cpu_baseline and args.routing == "token"
     if do_cpu:
         cpu_rows = {"worked-example-n64-f16384-gelu": 384, "prefill-n8-f14336": 128,
                     "zipf-skew-n128-k8": 4096, "decode-t32-n64-k8": 256}.get(w.name, 256)
@@ -313,7 +317,15 @@ def main():
     torch.cuda.synchronize()
 
     s = B.shape(w.T, w.d, w.N, w.k, w.F, w.act, w.dtype)
-    A = w.A
+    ec = args.routing == "expert"
+    C = max(1, w.T * w.k // w.N) if ec else 0
+    A = w.N * C if ec else w.A
+    s_rows = B.shape(A, w.d, w.N, 1, w.F, w.act, w.dtype) if ec else s     # grouped FFN over the N*C rows
+    s_slots = B.shape(w.T, w.d, w.N, w.N, w.F, w.act, w.dtype) if ec else s  # N (row, weight) slots per token
+    if ec:
+        probs = torch.empty((w.T, w.N), dtype=torch.float32, device="cuda")
+        inv_ec = torch.empty((w.T, w.N), dtype=torch.int32, device="cuda")
+        w_ec = torch.empty((w.T, w.N), dtype=torch.float32, device="cuda")
     idx = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
     tw = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
     counts = torch.empty(w.N, dtype=torch.int32, device="cuda")
@@ -325,22 +337,30 @@ def main():
     out = torch.empty((w.T, w.d), dtype=td, device="cuda")
     dropped = torch.zeros(1, dtype=torch.int32, device="cuda")
     cf = args.capacity_factor
-    ws = B.workspace(max(B.permute_workspace_size(s), B.grouped_ffn_workspace_size(s)))
+    ws = B.workspace(max(B.permute_workspace_size(s), B.grouped_ffn_workspace_size(s_rows)))
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
         if ev: ev[0].record(stream)
-        B.route(s, x, wg, bias, idx, tw)
+        if ec:
+            B.route_expert_choice(s, C, x, wg, bias, probs, perm, counts, offsets, inv_ec, w_ec)
+        else:
+            B.route(s, x, wg, bias, idx, tw)
         if ev: ev[1].record(stream)
-        if cf is None:
+        if ec:
+            B.gather_rows(s, inv_ec, w.N, A, x, xp)
+        elif cf is None:
             B.permute(s, idx, x, counts, offsets, perm, inv, xp, ws)
         else:
             B.permute_capacity(s, idx, x, cf, counts, offsets, perm, inv, xp, ws, dropped=dropped)
         if ev: ev[2].record(stream)
-        B.grouped_ffn(s, xp, offsets, WG, WU, WD, yp, ws)
+        B.grouped_ffn(s_rows, xp, offsets, WG, WU, WD, yp, ws)
         if ev: ev[3].record(stream)
-        B.combine(s, yp, inv, tw, out)
+        if ec:
+            B.combine(s_slots, yp, inv_ec, w_ec, out)
+        else:
+            B.combine(s, yp, inv, tw, out)
         if ev: ev[4].record(stream)
 
     for _ in range(args.warmup):
@@ -377,13 +397,17 @@ def main():
         x_host = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory() if w.dtype == "bf16" \
             else torch.from_numpy(x_h).pin_memory()
         out_host = torch.empty((w.T, w.d), dtype=td).pin_memory()
-        wsh = B.workspace(B.hostio_workspace_size(s))
+        wsh = B.workspace(B.expert_choice_workspace_size(s, C) if ec else B.hostio_workspace_size(s))
         del ws
 
         def forward_e2e():
-            if cf is None:
+            if ec:                             # no host-buffer entry for these: copies around the call
+                x.copy_(x_host, non_blocking=True)
+                B.forward_expert_choice(s, C, x, wg, bias, WG, WU, WD, out, wsh)
+                out_host.copy_(out, non_blocking=True)
+            elif cf is None:
                 B.forward_hostio(s, x_host, wg, bias, WG, WU, WD, out_host, wsh)
-            else:                              # no host-buffer entry with a capacity: copies around the call
+            else:
                 x.copy_(x_host, non_blocking=True)
                 B.forward_capacity(s, cf, x, wg, bias, WG, WU, WD, out, wsh)
                 out_host.copy_(out, non_blocking=True)
@@ -456,7 +480,8 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,
-                   "gate": "fp32", "ffn_tiling": args.ffn_tiling, "capacity_factor": cf, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "gate": "fp32", "ffn_tiling": args.ffn_tiling, "capacity_factor": cf,
+                   "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write); expert weights also exceed L2"},
         "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
@@ -465,7 +490,9 @@ def main():
         "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()),
         "dropped_assignments": int(dropped.item()) if cf is not None else 0,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 8 * args.steps,   # route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1
+        # token choice: route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1;
+        # expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
+        "gpu_launches": (6 if ec else 8) * args.steps,
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),
     }

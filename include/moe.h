@@ -211,6 +211,53 @@ moe_status moe_forward_ex(const moe_shape *s, const moe_options *opt, const void
                           int32_t *counts, void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Expert-choice routing: "MoE混合专家模型计算原理与推理部署实战解析" section
+ * 2.3 (each expert picks its own top tokens: every expert processes the same
+ * number, and a token may be picked by none). Readings: the affinity is the
+ * gate probability p[t,e] = softmax over the experts of the fp32 logits
+ * x w_g (+ bias, added to the logits); expert e takes the C tokens of
+ * largest p[t,e] (equal values: lower token id first) and weights each by
+ * p[t,e] (no renormalisation). s->k is not used (any valid value).
+ * Outputs:
+ *   probs   [T,N] fp32   the gate probabilities
+ *   perm    [N*C] int32  row -> token; expert e owns rows e*C .. e*C + C - 1,
+ *                        its tokens in ascending order
+ *   counts  [N]   = C;   offsets [N+1] = e*C
+ *   inv     [T,N] int32  row of (t, e), or -2 when e did not pick t
+ *   w       [T,N] fp32   p[t,e] when e picked t, else 0
+ * Needs 0 <= C <= T. The choice is deterministic (integer radix select).
+ */
+moe_status moe_route_expert_choice(const moe_shape *s, int64_t C, const void *x, const float *w_g,
+                                   const float *bias, float *probs, int32_t *perm, int32_t *counts,
+                                   int32_t *offsets, int32_t *inv, float *w, void *stream);
+
+/*
+ * The row copy of the grouping step on its own ("MoE混合专家模型计算原理与推理
+ * 部署实战解析" section 5.1 step 3): x_perm[inv[t*slots + j]] = x[t] for every
+ * t < T and j < slots whose row lies in [0, rows); other entries (-2: not
+ * chosen or dropped) are skipped. With the expert-choice tables (slots = N,
+ * rows = N*C) it builds the expert-choice x_perm; moe_grouped_ffn then runs
+ * on a shape with T = N*C, k = 1, and moe_combine on one with k = N.
+ * x [T,d], x_perm [rows, d] (dtype of s).
+ */
+moe_status moe_gather_rows(const moe_shape *s, const int32_t *inv, int32_t slots, int64_t rows,
+                           const void *x, void *x_perm, void *stream);
+
+/*
+ * The whole layer with expert-choice routing: moe_route_expert_choice, the
+ * row copy x_perm[row] = x[perm[row]], the grouped FFN over the N*C rows
+ * (C per expert), and out[t] = sum over the experts e that picked t of
+ * p[t,e] * y_e(x_t), summed in expert order (a token picked by no expert
+ * gets 0). counts [N] is optional. ws: moe_expert_choice_workspace_size(s, C)
+ * bytes.
+ */
+moe_status moe_forward_expert_choice(const moe_shape *s, int64_t C, const void *x, const float *w_g,
+                                     const float *bias, const void *w_gate, const void *w_up,
+                                     const void *w_down, void *out, int32_t *counts, void *ws,
+                                     size_t ws_bytes, void *stream);
+size_t moe_expert_choice_workspace_size(const moe_shape *s, int64_t C);
+
+/*
  * moe_forward with x and out in HOST memory (pinned memory makes the copies
  * asynchronous): copies x into ws, runs the layer, copies out back, all on
  * `stream`. The caller synchronises the stream before reading out_host.

@@ -56,6 +56,10 @@ SIGNATURES = {
     "moe_route_ex": (I32, [SP, P, P, P, I32, P, P, P, P, SZ, P]),
     "moe_route_ex_workspace_size": (SZ, [SP]),
     "moe_forward_ex": (I32, [SP, OP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_route_expert_choice": (I32, [SP, I64, P, P, P, P, P, P, P, P, P, P]),
+    "moe_forward_expert_choice": (I32, [SP, I64, P, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_expert_choice_workspace_size": (SZ, [SP, I64]),
+    "moe_gather_rows": (I32, [SP, P, I32, I64, P, P, P]),
     "moe_combine": (I32, [SP, P, P, P, P, P]),
     "moe_forward": (I32, [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_hostio": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
@@ -202,6 +206,27 @@ def forward_ex(s, x, w_g, bias, w_gate, w_up, w_down, out, ws, bias_mode="logits
     _check(lib().moe_forward_ex(ctypes.byref(s), ctypes.byref(o), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(w_gate),
                                 _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
                                 _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_ex")
+
+
+def gather_rows(s, inv, slots, rows, x, x_perm, stream=None):
+    _check(lib().moe_gather_rows(ctypes.byref(s), _ptr(inv), int(slots), int(rows), _ptr(x), _ptr(x_perm),
+                                 _stream(stream)), "moe_gather_rows")
+
+
+def expert_choice_workspace_size(s, C: int) -> int:
+    return lib().moe_expert_choice_workspace_size(ctypes.byref(s), int(C))
+
+
+def route_expert_choice(s, C, x, w_g, bias, probs, perm, counts, offsets, inv, w, stream=None):
+    _check(lib().moe_route_expert_choice(ctypes.byref(s), int(C), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(probs),
+                                         _ptr(perm), _ptr(counts), _ptr(offsets), _ptr(inv), _ptr(w),
+                                         _stream(stream)), "moe_route_expert_choice")
+
+
+def forward_expert_choice(s, C, x, w_g, bias, w_gate, w_up, w_down, out, ws, counts=None, stream=None):
+    _check(lib().moe_forward_expert_choice(ctypes.byref(s), int(C), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(w_gate),
+                                           _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(counts), _ptr(ws), ws.numel(),
+                                           _stream(stream)), "moe_forward_expert_choice")
 
 
 def permute_capacity(s, topk_idx, x, capacity_factor, counts, offsets, perm, inv_perm, x_perm, ws, dropped=None,

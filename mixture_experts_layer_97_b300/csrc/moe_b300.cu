@@ -15,6 +15,7 @@
 
 #include "combine.cuh"
 #include "common.cuh"
+#include "expert_choice.cuh"
 #include "ffn_simt.cuh"
 #include "ffn_tc.cuh"
 #include "ffn_tc_swap.cuh"
@@ -159,6 +160,7 @@ struct RouteArgs {
   float* w;
   float* stats_part;   // [grid][2N + 1] or null
   int64_t rows;
+  float* probs_out;    // [T, N] or null
 };
 
 template <int EG, int EPT, int TPT, typename TX>
@@ -172,7 +174,8 @@ moe_status launch_route_cfg(const moe_shape* s, const TX* x, RouteArgs& a, cudaS
   const int64_t grid = (s->T + Cfg::TM - 1) / Cfg::TM;
   a.rows = grid;
   kern<<<static_cast<unsigned>(grid), kRouteThreads, Cfg::kSmem, st>>>(
-      x, a.wg, a.bias, static_cast<int>(s->T), s->d, s->N, s->k, a.bias_select, a.idx, a.w, a.stats_part);
+      x, a.wg, a.bias, static_cast<int>(s->T), s->d, s->N, s->k, a.bias_select, a.idx, a.w, a.stats_part,
+      a.probs_out);
   return launched();
 }
 
@@ -220,7 +223,7 @@ moe_status launch_route(const moe_shape* s, const TX* x, RouteArgs& a, cudaStrea
 // route kernel left in stats_ws.
 moe_status route_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, int32_t* idx, float* w,
                       cudaStream_t st, int bias_select = 0, float* load_stats = nullptr, void* stats_ws = nullptr) {
-  RouteArgs a{wg, bias, bias_select, idx, w, load_stats ? static_cast<float*>(stats_ws) : nullptr, 0};
+  RouteArgs a{wg, bias, bias_select, idx, w, load_stats ? static_cast<float*>(stats_ws) : nullptr, 0, nullptr};
   moe_status r = s->dtype == MOE_BF16
                      ? launch_route<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(x), a, st)
                      : launch_route<float>(s, static_cast<const float*>(x), a, st);
@@ -230,6 +233,17 @@ moe_status route_impl(const moe_shape* s, const void* x, const float* wg, const 
 }
 
 // ---------------------------------------------------------------- permute
+// x_perm[inv[t*k + j]] = x[t] for every j < k whose row is in [0, A).
+moe_status launch_row_copy(const moe_shape* s, const int32_t* inv, const void* x, int k, int64_t A, void* x_perm,
+                           cudaStream_t st) {
+  if (s->T == 0) return MOE_OK;
+  const int64_t nv = static_cast<int64_t>(s->d) * esize(s) / 16;
+  const int64_t warps = s->T * copy_groups(nv);
+  permute_copy_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(
+      inv, static_cast<const uint4*>(x), s->T, k, A, nv, static_cast<uint4*>(x_perm));
+  return launched();
+}
+
 
 moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, int32_t* counts, int32_t* offsets,
                         int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, cudaStream_t st,
@@ -246,11 +260,7 @@ moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, i
     permute_rank_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, hist, offsets, s->T, s->N, s->k,
                                                                             capacity, perm, inv_perm, dropped);
     if (launched() != MOE_OK) return MOE_ERR_CUDA;
-    const int64_t nv = static_cast<int64_t>(s->d) * esize(s) / 16;
-    const int64_t warps = s->T * copy_groups(nv);
-    permute_copy_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(
-        inv_perm, static_cast<const uint4*>(x), s->T, s->k, n_assign(s), nv, static_cast<uint4*>(x_perm));
-    if (launched() != MOE_OK) return MOE_ERR_CUDA;
+    return launch_row_copy(s, inv_perm, x, s->k, n_assign(s), x_perm, st);
   }
   return MOE_OK;
 }
@@ -448,6 +458,91 @@ moe_status forward_impl(const moe_shape* s, const void* x, const float* wg, cons
   return combine_impl(s, b.y_perm, b.inv_perm, w, out, st);
 }
 
+// ---------------------------------------------------------------- expert choice
+// Shapes of the expert-choice path: C tokens per expert, N*C rows; every
+// token has N (row, weight) slots, so the row copy and the combine run as a
+// top-k with k = N.
+moe_status ec_shape_status(const moe_shape* s, int64_t C) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  if (C < 0 || C > s->T) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s->N) * C >= (int64_t(1) << 31) || s->T * s->N >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_shape ec_ffn_shape(const moe_shape* s, int64_t C) {
+  moe_shape f = *s;
+  f.T = static_cast<int64_t>(s->N) * C;
+  f.k = 1;
+  return f;
+}
+
+moe_shape ec_slot_shape(const moe_shape* s) {
+  moe_shape c = *s;
+  c.k = s->N;
+  return c;
+}
+
+struct EcBufs {
+  float* probs;
+  int32_t* inv;
+  float* w;
+  int32_t* perm;
+  int32_t* counts;
+  int32_t* offsets;
+  void* x_perm;
+  void* y_perm;
+  void* ffn_ws;
+  size_t total;
+};
+
+EcBufs carve_ec(const moe_shape* s, int64_t C, void* ws) {
+  Carve c(ws);
+  EcBufs b{};
+  const size_t TN = static_cast<size_t>(s->T) * s->N;
+  const size_t rows = static_cast<size_t>(s->N) * C;
+  const moe_shape f = ec_ffn_shape(s, C);
+  b.probs = c.take<float>(sizeof(float) * TN);
+  b.inv = c.take<int32_t>(sizeof(int32_t) * TN);
+  b.w = c.take<float>(sizeof(float) * TN);
+  b.perm = c.take<int32_t>(sizeof(int32_t) * rows);
+  b.counts = c.take<int32_t>(sizeof(int32_t) * s->N);
+  b.offsets = c.take<int32_t>(sizeof(int32_t) * (s->N + 1));
+  b.x_perm = c.take<uint8_t>(esize(s) * rows * s->d);
+  b.y_perm = c.take<uint8_t>(esize(s) * rows * s->d);
+  b.ffn_ws = c.take<uint8_t>(ffn_ws(&f));
+  b.total = c.used;
+  return b;
+}
+
+moe_status ec_route_impl(const moe_shape* s, int64_t C, const void* x, const float* wg, const float* bias,
+                         float* probs, int32_t* perm, int32_t* counts, int32_t* offsets, int32_t* inv, float* w,
+                         cudaStream_t st) {
+  RouteArgs a{wg, bias, 0, nullptr, nullptr, nullptr, 0, probs};
+  moe_status r = s->dtype == MOE_BF16
+                     ? launch_route<__nv_bfloat16>(s, static_cast<const __nv_bfloat16*>(x), a, st)
+                     : launch_route<float>(s, static_cast<const float*>(x), a, st);
+  if (r != MOE_OK) return r;
+  ec_select_kernel<<<static_cast<unsigned>(s->N), kEcThreads, 0, st>>>(probs, s->T, s->N, C, perm, counts, offsets,
+                                                                       inv, w);
+  return launched();
+}
+
+moe_status ec_forward_impl(const moe_shape* s, int64_t C, const void* x, const float* wg, const float* bias,
+                           const void* w_gate, const void* w_up, const void* w_down, void* out, const EcBufs& b,
+                           cudaStream_t st) {
+  moe_status r = ec_route_impl(s, C, x, wg, bias, b.probs, b.perm, b.counts, b.offsets, b.inv, b.w, st);
+  if (r != MOE_OK) return r;
+  const moe_shape slots = ec_slot_shape(s);
+  const moe_shape f = ec_ffn_shape(s, C);
+  r = launch_row_copy(s, b.inv, x, s->N, f.T, b.x_perm, st);
+  if (r != MOE_OK) return r;
+  r = ffn_impl(&f, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st);
+  if (r != MOE_OK) return r;
+  return combine_impl(&slots, b.y_perm, b.inv, b.w, out, st);
+}
+
 bool weights_ok(const moe_shape* s, const void* w_gate, const void* w_up, const void* w_down) {
   if (!ptr_ok(w_gate, true) || !ptr_ok(w_down, true)) return false;
   if (s->act == MOE_SWIGLU) return ptr_ok(w_up, true);
@@ -628,6 +723,48 @@ moe_status moe_forward_ex(const moe_shape* s, const moe_options* opt, const void
   if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
   return forward_impl(s, x, w_g, bias, w_gate, w_up, w_down, out, topk_idx, topk_w, counts, b,
                       static_cast<cudaStream_t>(stream), o);
+}
+
+moe_status moe_gather_rows(const moe_shape* s, const int32_t* inv, int32_t slots, int64_t rows, const void* x,
+                           void* x_perm, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  if (slots < 1 || rows < 0 || s->T * static_cast<int64_t>(slots) >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
+  const bool any = s->T > 0;
+  if (!ptr_ok(inv, any) || !ptr_ok(x, any) || !ptr_ok(x_perm, any && rows > 0)) return MOE_ERR_INVALID_ARG;
+  return launch_row_copy(s, inv, x, slots, rows, x_perm, static_cast<cudaStream_t>(stream));
+}
+
+size_t moe_expert_choice_workspace_size(const moe_shape* s, int64_t C) {
+  return ec_shape_status(s, C) == MOE_OK ? carve_ec(s, C, nullptr).total : 0;
+}
+
+moe_status moe_route_expert_choice(const moe_shape* s, int64_t C, const void* x, const float* w_g, const float* bias,
+                                   float* probs, int32_t* perm, int32_t* counts, int32_t* offsets, int32_t* inv,
+                                   float* w, void* stream) {
+  moe_status st = ec_shape_status(s, C);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(x, any) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) || !ptr_ok(probs, any) ||
+      !ptr_ok(perm, C > 0) || !ptr_ok(counts, true) || !ptr_ok(offsets, true) || !ptr_ok(inv, any) ||
+      !ptr_ok(w, any))
+    return MOE_ERR_INVALID_ARG;
+  return ec_route_impl(s, C, x, w_g, bias, probs, perm, counts, offsets, inv, w, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_expert_choice(const moe_shape* s, int64_t C, const void* x, const float* w_g,
+                                     const float* bias, const void* w_gate, const void* w_up, const void* w_down,
+                                     void* out, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = ec_shape_status(s, C);
+  if (st != MOE_OK) return st;
+  const bool any = s->T > 0;
+  if (!ptr_ok(x, any) || !ptr_ok(w_g, true) || !ptr_ok(bias, false) || !weights_ok(s, w_gate, w_up, w_down) ||
+      !ptr_ok(out, any) || !ptr_ok(counts, false) || !ptr_ok(ws, true))
+    return MOE_ERR_INVALID_ARG;
+  EcBufs b = carve_ec(s, C, ws);
+  if (ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  if (counts != nullptr) b.counts = counts;
+  return ec_forward_impl(s, C, x, w_g, bias, w_gate, w_up, w_down, out, b, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_forward_hostio(const moe_shape* s, const void* x_host, const float* w_g, const float* bias,

@@ -25,6 +25,10 @@
 // "这不是“参数越多越强”的简单故事" sections 3.1 and 4.4. No float atomics: the
 // statistics are reproducible bit for bit.
 //
+// Gate probabilities (optional, for expert-choice routing): probs_out [T,N]
+// receives the full softmax p[t,:] in fp32; with topk_idx == null the top-k
+// step is skipped.
+//
 // Each logit is the sequential FMA chain over i = 0..d-1 in index order (one
 // thread owns it from start to end), then one fp32 bias add: the plainest fp32
 // evaluation, so the top-k decision is reproducible bit for bit.
@@ -90,7 +94,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
                                                               int k, int bias_select,
                                                               int32_t* __restrict__ topk_idx,
                                                               float* __restrict__ topk_w,
-                                                              float* __restrict__ stats_part) {
+                                                              float* __restrict__ stats_part,
+                                                              float* __restrict__ probs_out) {
   using C = RouteCfg<EG, EPT, TPT, TX>;
   constexpr int NP = C::NP, TM = C::TM, S = C::STAGES;
   constexpr int NPR = NP < 32 ? 32 : NP;   // register slots per token for the argmax
@@ -232,42 +237,63 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
       v[m] = (n < N) ? g[m] + bsel[m] : -INFINITY;
       taken[m] = (n >= N);
     }
-    float sel_v[SLOTS];
-    int sel_i[SLOTS];
+    if (topk_idx != nullptr) {   // top-k choice and its renormalised weights
+      float sel_v[SLOTS];
+      int sel_i[SLOTS];
 #pragma unroll
-    for (int m = 0; m < SLOTS; ++m) { sel_v[m] = -INFINITY; sel_i[m] = 0; }
-    float top = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7FFFFFFF;
+      for (int m = 0; m < SLOTS; ++m) { sel_v[m] = -INFINITY; sel_i[m] = 0; }
+      float top = 0.f;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
 #pragma unroll
-      for (int m = 0; m < SLOTS; ++m) {
-        const int n = lane + 32 * m;
-        if (!taken[m] && (v[m] > bv || (v[m] == bv && n < bi))) { bv = v[m]; bi = n; }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
-      // the winner's softmax logit (its score unless the bias only chooses)
-      float gw = -INFINITY;
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m)
-        if ((bi >> 5) == m) gw = g[m];
-      gw = __shfl_sync(0xffffffffu, gw, bi & 31);
-      top = (j == 0) ? gw : fmaxf(top, gw);
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m) {
-        if (bi == lane + 32 * m) {
-          taken[m] = true;
-          c_acc[m] += 1.f;
+        for (int m = 0; m < SLOTS; ++m) {
+          const int n = lane + 32 * m;
+          if (!taken[m] && (v[m] > bv || (v[m] == bv && n < bi))) { bv = v[m]; bi = n; }
         }
-        if ((j & 31) == lane && (j >> 5) == m) { sel_v[m] = gw; sel_i[m] = bi; }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        // the winner's softmax logit (its score unless the bias only chooses)
+        float gw = -INFINITY;
+#pragma unroll
+        for (int m = 0; m < SLOTS; ++m)
+          if ((bi >> 5) == m) gw = g[m];
+        gw = __shfl_sync(0xffffffffu, gw, bi & 31);
+        top = (j == 0) ? gw : fmaxf(top, gw);
+#pragma unroll
+        for (int m = 0; m < SLOTS; ++m) {
+          if (bi == lane + 32 * m) {
+            taken[m] = true;
+            c_acc[m] += 1.f;
+          }
+          if ((j & 31) == lane && (j >> 5) == m) { sel_v[m] = gw; sel_i[m] = bi; }
+        }
+      }
+      float part = 0.f;
+      float ex[SLOTS];
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) {
+        const int j = lane + 32 * m;
+        ex[m] = (j < k) ? expf(sel_v[m] - top) : 0.f;
+        part += ex[m];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      const float inv = 1.f / part;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) {
+        const int j = lane + 32 * m;
+        if (j < k) {
+          topk_idx[t * k + j] = sel_i[m];
+          topk_w[t * k + j] = ex[m] * inv;
+        }
       }
     }
-    if (want_stats) {         // full softmax over the N experts
+    if (want_stats || probs_out != nullptr) {   // full softmax over the N experts
       float gmax = -INFINITY;
 #pragma unroll
       for (int m = 0; m < SLOTS; ++m) gmax = fmaxf(gmax, g[m]);
@@ -283,27 +309,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
       const float iz = 1.f / z;
 #pragma unroll
-      for (int m = 0; m < SLOTS; ++m) p_acc[m] += e[m] * iz;
-      top1_acc += iz;         // p of the largest logit is exp(0) / z
-    }
-    float part = 0.f;
-    float ex[SLOTS];
-#pragma unroll
-    for (int m = 0; m < SLOTS; ++m) {
-      const int j = lane + 32 * m;
-      ex[m] = (j < k) ? expf(sel_v[m] - top) : 0.f;
-      part += ex[m];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    const float inv = 1.f / part;
-#pragma unroll
-    for (int m = 0; m < SLOTS; ++m) {
-      const int j = lane + 32 * m;
-      if (j < k) {
-        topk_idx[t * k + j] = sel_i[m];
-        topk_w[t * k + j] = ex[m] * inv;
+      for (int m = 0; m < SLOTS; ++m) {
+        const int n = lane + 32 * m;
+        p_acc[m] += e[m] * iz;
+        if (probs_out != nullptr && n < N) probs_out[t * N + n] = e[m] * iz;
       }
+      top1_acc += iz;         // p of the largest logit is exp(0) / z
     }
   }
   if (!want_stats) return;

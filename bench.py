@@ -448,7 +448,8 @@ def main():
     # active experts' weights. Both fractions are reported.
     rows_per_active = rows / max(1, int((cnt > 0).sum()))
     tensor_bound = rows_per_active >= 128
-    traffic = recorded_traffic(w.name)
+    # the record is for the plain token-choice call; other routings move other bytes
+    traffic = recorded_traffic(w.name) if (not ec and cf is None) else None
     tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
     gbs = wbytes / (ffn_ms * 1e-3) / 1e9
     if tensor_bound:

@@ -257,7 +257,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens"],
+    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs"],
                     help="tensor-core tiling of the grouped GEMMs (library default: auto)")
     ap.add_argument("--capacity-factor", type=float, default=None,
                     help="expert capacity ceil(cf * T * k / N); overflow assignments are dropped")

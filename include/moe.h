@@ -305,13 +305,17 @@ moe_status moe_permute_noalloc(const moe_shape *s, const int32_t *topk_idx, cons
  *   MOE_TILING_TOKENS  128 weight rows x up to 256 tokens per tile (tokens are
  *                      the MMA's N side, tiles balanced per expert and rounded
  *                      to 16 rows): little padding when experts hold few rows.
+ *   MOE_TILING_PAIRS   token tiles computed by clusters of two SMs sharing each
+ *                      MMA (256 weight rows per MMA, each SM holding half of
+ *                      the tile's tokens): four 48 KB pipeline stages per SM
+ *                      instead of three 64 KB ones.
  *   MOE_TILING_AUTO    per GEMM: token tiles when T*k >= 64*N and the GEMM's
  *                      reduction length (d for the first, F for the second)
  *                      is >= 4096, else row tiles (default).
  * The pages' grouped GEMM ("MoE显存与计算开销四阶段手算指南" section 4.3)
  * fixes no tiling; this only chooses how the same product is blocked.
  */
-typedef enum { MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2 } moe_tiling;
+typedef enum { MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2, MOE_TILING_PAIRS = 3 } moe_tiling;
 moe_status moe_set_ffn_tiling(int mode);
 int moe_get_ffn_tiling(void);
 

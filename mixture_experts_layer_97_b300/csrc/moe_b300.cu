@@ -19,6 +19,7 @@
 #include "ffn_simt.cuh"
 #include "ffn_tc.cuh"
 #include "ffn_tc_swap.cuh"
+#include "ffn_tc_pair.cuh"
 #include "permute.cuh"
 #include "route.cuh"
 
@@ -291,6 +292,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Tiling of the bf16 grouped GEMMs (moe_set_ffn_tiling), process wide.
+std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
+
 // bf16 matrix [rows, cols] row-major; box = box_rows x box_cols columns with the
 // swizzle whose span is one box row (box_cols * 2 bytes: 128 or 64).
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
@@ -364,14 +368,58 @@ moe_status launch_tc_swap_bk(const moe_shape* s, const void* a, int K, const voi
   return launched();
 }
 
+// The token-tile grouped GEMM on SM pairs: clusters of two CTAs sharing
+// each MMA (tcgen05 cta_group::2).
+template <int EPI>
+moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
+                          const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  constexpr int OFP = pr_tile_features<EPI>();
+  const int64_t A = n_assign(s);
+  CUtensorMap mx, mw0, mw1;
+  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox, kTcBK)) return MOE_ERR_CUDA;
+  const uint64_t wrows = static_cast<uint64_t>(s->N) * Nout;
+  if (!make_map(&mw0, w0, wrows, static_cast<uint64_t>(K), kSwFM, kTcBK)) return MOE_ERR_CUDA;
+  if (EPI == EPI_SWIGLU) {
+    if (!make_map(&mw1, w1, wrows, static_cast<uint64_t>(K), kSwFM, kTcBK)) return MOE_ERR_CUDA;
+  } else {
+    mw1 = mw0;
+  }
+  auto kern = grouped_gemm_tc_pair_kernel<EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPrSmemBytes)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int64_t n_ftiles = (Nout + OFP - 1) / OFP;
+  const int64_t pairs_needed = ((A + kSwMaxNT - 1) / kSwMaxNT + s->N) * n_ftiles;
+  const int64_t max_pairs = num_sms() / 2;
+  const int64_t pairs = pairs_needed < max_pairs ? pairs_needed : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kSwThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPrSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, mw0, mw1, mx, offsets, s->N, static_cast<int>(A), K, Nout,
+                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launched();
+}
+
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  if (g_ffn_tiling.load(std::memory_order_relaxed) == MOE_TILING_PAIRS)
+    return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
   return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
 }
 
 // Process-wide choice between the two tensor-core tilings (moe_set_ffn_tiling).
-std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
+
 
 // K is the reduction length of the GEMM in question (d for the first, F for
 // the second). Token tiles pad less but keep one accumulator pair in TMEM, so
@@ -379,7 +427,7 @@ std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
 // expert holds enough rows to fill tiles and K is long enough to hide it.
 bool use_token_tiles(const moe_shape* s, int K) {
   const int mode = g_ffn_tiling.load(std::memory_order_relaxed);
-  if (mode == MOE_TILING_TOKENS) return true;
+  if (mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS) return true;
   if (mode == MOE_TILING_ROWS) return false;
   return n_assign(s) >= static_cast<int64_t>(kAutoTokenTileMinRowsPerExpert) * s->N && K >= kAutoTokenTileMinK;
 }
@@ -816,7 +864,8 @@ moe_status moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, cons
 }
 
 moe_status moe_set_ffn_tiling(int mode) {
-  if (mode != MOE_TILING_AUTO && mode != MOE_TILING_ROWS && mode != MOE_TILING_TOKENS) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_TILING_AUTO && mode != MOE_TILING_ROWS && mode != MOE_TILING_TOKENS && mode != MOE_TILING_PAIRS)
+    return MOE_ERR_INVALID_ARG;
   g_ffn_tiling.store(mode, std::memory_order_relaxed);
   return MOE_OK;
 }

@@ -64,7 +64,7 @@ RAGGED = [0, 1, 127, 128, 129, 300, 0, 5]
 RAGGED_TOKENS = [16, 17, 256, 257, 0, 31, 513, 1500]
 
 
-@pytest.fixture(params=["rows", "tokens"])
+@pytest.fixture(params=["rows", "tokens", "pairs"])
 def tiling(request):
     B.set_ffn_tiling(request.param)
     yield request.param
@@ -170,7 +170,7 @@ def test_tilings_agree_within_tolerance():
     of each other."""
     w, xp, ws, off = make_case([200, 0, 300, 45, 1000], 512, 384, "swiglu", "bf16", 12)
     outs = {}
-    for mode in ("rows", "tokens"):
+    for mode in ("rows", "tokens", "pairs"):
         B.set_ffn_tiling(mode)
         outs[mode] = run_ffn(w, xp, ws, off)
     B.set_ffn_tiling("auto")
@@ -178,3 +178,4 @@ def test_tilings_agree_within_tolerance():
     for mode, got in outs.items():
         assert rel_err(got, ref) <= tol("bf16"), mode
     assert rel_err(outs["rows"], outs["tokens"]) <= tol("bf16")
+    assert rel_err(outs["pairs"], outs["tokens"]) <= tol("bf16")

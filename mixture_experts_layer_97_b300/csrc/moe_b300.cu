@@ -413,9 +413,10 @@ moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* 
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
-  if (g_ffn_tiling.load(std::memory_order_relaxed) == MOE_TILING_PAIRS)
-    return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
-  return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
+  // auto and "pairs" run token tiles on SM pairs; "tokens" keeps them on single SMs
+  if (g_ffn_tiling.load(std::memory_order_relaxed) == MOE_TILING_TOKENS)
+    return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
+  return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
 }
 
 // Process-wide choice between the two tensor-core tilings (moe_set_ffn_tiling).

@@ -439,7 +439,41 @@ def main():
         e_ms = max_over_ranks(e_ms, dist, "cuda")
         io = w.T * w.d * w.esize
         e2e = {"value": job_throughput(w.T, world, e_ms), "unit": "tokens/s", "h2d_bytes_per_step": io,
-               "d2h_bytes_per_step": io, "ms_per_step": e_ms}
+               "d2h_bytes_per_step": io, "ms_per_step": e_ms,
+               "mode": "serial: each step copies x in, runs the layer, copies out (moe_forward_hostio)"}
+        if not ec and cf is None:
+            # the same steps through moe_forward_hostio_pipelined: step i+1's input copy and step i-1's
+            # output copy run on their own streams while step i's layer runs
+            del wsh
+            wsp = B.workspace(B.hostio_pipelined_workspace_size(s))
+            outs_h = [out_host, torch.empty((w.T, w.d), dtype=td).pin_memory()]
+            s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+            def piped(i):
+                B.forward_hostio_pipelined(s, x_host, wg, bias, WG, WU, WD, outs_h[i % 2], wsp, i % 2, stream,
+                                           s_in, s_out)
+
+            for i in range(2):
+                piped(i)
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            flush_l2()
+            torch.cuda.synchronize()
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            s_in.wait_event(p0)
+            for i in range(args.steps):
+                piped(i)
+            p1.record(s_out)                   # after the last output copy
+            torch.cuda.synchronize()
+            if B.get_error() != B.MOE_OK:
+                raise RuntimeError("device error during the pipelined end-to-end run")
+            p_ms = max_over_ranks(p0.elapsed_time(p1) / args.steps, dist, "cuda")
+            e2e.update({"value": job_throughput(w.T, world, p_ms), "ms_per_step": p_ms,
+                        "mode": ("pipelined: moe_forward_hostio_pipelined over consecutive steps; every step "
+                                 "copies its x in and its output out, overlapping the neighbouring steps' layer"),
+                        "serial_value": job_throughput(w.T, world, e_ms), "serial_ms_per_step": e_ms})
 
     if rank != 0:
         if dist:

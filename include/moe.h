@@ -269,6 +269,32 @@ moe_status moe_forward_hostio(const moe_shape *s, const void *x_host, const floa
                               void *stream);
 
 /*
+ * moe_forward_hostio for a sequence of batches, with the copies of one batch
+ * overlapping the layer of another: three streams (compute_stream for the
+ * layer, h2d_stream for the x copies, d2h_stream for the output copies) and
+ * two workspace slots, alternated by the caller (slot = 0, 1, 0, 1, ... on
+ * consecutive calls, from one host thread). The call only enqueues work:
+ *   h2d_stream:     x_host -> slot's x once the call two back stopped reading it
+ *   compute_stream: the layer on the slot's x once it is in and the slot's
+ *                   previous output has been copied out
+ *   d2h_stream:     the slot's out -> out_host
+ * out_host holds this batch's output once d2h_stream has passed this call
+ * (synchronise it, or an event recorded on it after the call); x_host must
+ * stay unchanged until h2d_stream has passed the call. Device inputs
+ * (weights, w_g, bias) must not change while calls are in flight. The
+ * library creates eight events per device on first use (kept until the
+ * process exits). ws: moe_forward_hostio_pipelined_workspace_size(s) bytes.
+ * The pages name no such entry point: it exists so that host<->device copies
+ * of consecutive batches hide behind the layer.
+ */
+moe_status moe_forward_hostio_pipelined(const moe_shape *s, const void *x_host, const float *w_g,
+                                        const float *bias, const void *w_gate, const void *w_up,
+                                        const void *w_down, void *out_host, void *ws, size_t ws_bytes,
+                                        int32_t slot, void *compute_stream, void *h2d_stream,
+                                        void *d2h_stream);
+size_t moe_forward_hostio_pipelined_workspace_size(const moe_shape *s);
+
+/*
  * moe_permute without a caller workspace. No passage of the pages has a
  * counterpart: this exists for callers that cannot hand the library device
  * scratch memory -- for example a host framework that gives a custom operator
@@ -309,9 +335,10 @@ moe_status moe_permute_noalloc(const moe_shape *s, const int32_t *topk_idx, cons
  *                      MMA (256 weight rows per MMA, each SM holding half of
  *                      the tile's tokens): four 48 KB pipeline stages per SM
  *                      instead of three 64 KB ones.
- *   MOE_TILING_AUTO    per GEMM: token tiles on SM pairs when T*k >= 64*N and
- *                      the GEMM's reduction length (d for the first, F for the
- *                      second) is >= 4096, else row tiles (default).
+ *   MOE_TILING_AUTO    per GEMM: token tiles when T*k >= 64*N and the GEMM's
+ *                      reduction length (d for the first, F for the second) is
+ *                      >= 4096 -- on SM pairs while T*k < 512*N, else on single
+ *                      SMs -- and row tiles otherwise (default).
  * The pages' grouped GEMM ("MoE显存与计算开销四阶段手算指南" section 4.3)
  * fixes no tiling; this only chooses how the same product is blocked.
  */

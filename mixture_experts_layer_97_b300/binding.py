@@ -63,6 +63,8 @@ SIGNATURES = {
     "moe_combine": (I32, [SP, P, P, P, P, P]),
     "moe_forward": (I32, [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_hostio": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
+    "moe_forward_hostio_pipelined": (I32, [SP, P, P, P, P, P, P, P, P, SZ, I32, P, P, P]),
+    "moe_forward_hostio_pipelined_workspace_size": (SZ, [SP]),
     "moe_workspace_size": (SZ, [SP]),
     "moe_forward_hostio_workspace_size": (SZ, [SP]),
     "moe_permute_workspace_size": (SZ, [SP]),
@@ -260,6 +262,19 @@ def forward(s, x, w_g, bias, w_gate, w_up, w_down, out, ws, topk_idx=None, topk_
     _check(lib().moe_forward(ctypes.byref(s), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(w_gate), _ptr(w_up),
                              _ptr(w_down), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts), _ptr(ws),
                              ws.numel(), _stream(stream)), "moe_forward")
+
+
+def hostio_pipelined_workspace_size(s) -> int:
+    return lib().moe_forward_hostio_pipelined_workspace_size(ctypes.byref(s))
+
+
+def forward_hostio_pipelined(s, x_host, w_g, bias, w_gate, w_up, w_down, out_host, ws, slot, compute_stream,
+                             h2d_stream, d2h_stream):
+    _check(lib().moe_forward_hostio_pipelined(ctypes.byref(s), _host_ptr(x_host), _ptr(w_g), _ptr(bias),
+                                              _ptr(w_gate), _ptr(w_up), _ptr(w_down), _host_ptr(out_host),
+                                              _ptr(ws), ws.numel(), int(slot), _stream(compute_stream),
+                                              _stream(h2d_stream), _stream(d2h_stream)),
+           "moe_forward_hostio_pipelined")
 
 
 def forward_hostio(s, x_host, w_g, bias, w_gate, w_up, w_down, out_host, ws, stream=None):

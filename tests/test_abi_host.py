@@ -136,3 +136,14 @@ def test_tiling_policy_setter(L):
         assert B.get_ffn_tiling() == m
     assert L.moe_set_ffn_tiling(7) == B.MOE_ERR_INVALID_ARG
     assert B.get_ffn_tiling() == "auto"
+
+
+def test_pipelined_hostio_checks(L):
+    s = S()
+    p = ctypes.c_void_p(0x1000)
+    need = B.hostio_pipelined_workspace_size(s)
+    assert need >= B.workspace_size(s) + 4 * 64 * 256 * 2
+    st = L.moe_forward_hostio_pipelined(ctypes.byref(s), p, p, None, p, p, p, p, p, need, 2, None, None, None)
+    assert st == B.MOE_ERR_INVALID_ARG          # slot must be 0 or 1
+    st = L.moe_forward_hostio_pipelined(ctypes.byref(s), p, p, None, p, p, p, p, p, need - 1, 0, None, None, None)
+    assert st == B.MOE_ERR_WORKSPACE

@@ -101,6 +101,33 @@ def test_forward_hostio_matches_device_forward():
     assert torch.equal(out_host, out_dev.cpu())
 
 
+def test_forward_hostio_pipelined_matches_device_forward():
+    """Consecutive batches through the three-stream pipelined call, slots
+    alternating: every batch's host output equals the device forward's."""
+    w = SMALL[1]
+    inp = Inputs(w)
+    s = inp.shape
+    nb = 5
+    xs = [(inp.x.float() * (1.0 + 0.25 * i)).to(torch.bfloat16) for i in range(nb)]
+    refs = []
+    for xb in xs:
+        o = new((w.T, w.d), w.dtype)
+        B.forward(s, xb, inp.wg, inp.bias, inp.w_gate, inp.w_up, inp.w_down, o, B.workspace(B.workspace_size(s)))
+        refs.append(o)
+    torch.cuda.synchronize()
+    x_hosts = [xb.cpu().pin_memory() for xb in xs]
+    outs = [torch.full((w.T, w.d), 7.0, dtype=torch.bfloat16).pin_memory() for _ in xs]
+    ws = B.workspace(B.hostio_pipelined_workspace_size(s))
+    comp, h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for i in range(nb):
+        B.forward_hostio_pipelined(s, x_hosts[i], inp.wg, inp.bias, inp.w_gate, inp.w_up, inp.w_down, outs[i], ws,
+                                   i % 2, comp, h2d, d2h)
+    torch.cuda.synchronize()
+    assert B.get_error() == B.MOE_OK
+    for i in range(nb):
+        assert torch.equal(outs[i], refs[i].cpu()), i
+
+
 # ---------------------------------------------------------------- full size
 def staged_forward(inp: Inputs):
     """The four C-ABI calls with every intermediate in caller buffers."""

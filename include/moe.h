@@ -335,10 +335,9 @@ moe_status moe_permute_noalloc(const moe_shape *s, const int32_t *topk_idx, cons
  *                      MMA (256 weight rows per MMA, each SM holding half of
  *                      the tile's tokens): four 48 KB pipeline stages per SM
  *                      instead of three 64 KB ones.
- *   MOE_TILING_AUTO    per GEMM: token tiles when T*k >= 64*N and the GEMM's
- *                      reduction length (d for the first, F for the second) is
- *                      >= 4096 -- on SM pairs while T*k < 512*N, else on single
- *                      SMs -- and row tiles otherwise (default).
+ *   MOE_TILING_AUTO    per GEMM: token tiles on SM pairs when T*k >= 64*N and
+ *                      the GEMM's reduction length (d for the first, F for the
+ *                      second) is >= 4096, else row tiles (default).
  * The pages' grouped GEMM ("MoE显存与计算开销四阶段手算指南" section 4.3)
  * fixes no tiling; this only chooses how the same product is blocked.
  */

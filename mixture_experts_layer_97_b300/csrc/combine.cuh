@@ -55,7 +55,11 @@ struct Vec8<float> {
 template <int CPT>
 __host__ __device__ inline int combine_groups(int nchunk) { return (nchunk + 32 * CPT - 1) / (32 * CPT); }
 
-template <typename T, int CPT>
+// KMAX > 0: k <= KMAX, and the k (row, weight) pairs and then all k rows'
+// chunks are loaded before any is summed, so a lane has k * CPT row loads in
+// flight; KMAX = 0: any k, one row after the other (the expert-choice path,
+// where k is the number of experts and most slots are empty).
+template <typename T, int CPT, int KMAX>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __restrict__ y_perm,
                                                                   const int32_t* __restrict__ inv_perm,
                                                                   const float* __restrict__ topk_w, int64_t T_tok,
@@ -73,6 +77,41 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __res
   for (int u = 0; u < CPT; ++u)
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[u][e] = 0.f;
+  if constexpr (KMAX > 0) {
+    int64_t row[KMAX];
+    float wt[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      row[j] = j < k ? inv_perm[t * k + j] : -2;
+      wt[j] = j < k ? topk_w[t * k + j] : 0.f;
+    }
+    uint4 q[KMAX][CPT];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const bool live = row[j] >= 0 && row[j] < A;
+      if (row[j] != -2 && !live && c0 == 0) record_error(MOE_ERR_CORRUPT);
+      const T* yr = y_perm + (live ? row[j] : 0) * d;
+#pragma unroll
+      for (int u = 0; u < CPT; ++u) {
+        const int c = c0 + 32 * u;
+        q[j][u] = (live && c < nchunk) ? *reinterpret_cast<const uint4*>(yr + static_cast<int64_t>(c) * E)
+                                       : make_uint4(0, 0, 0, 0);
+      }
+    }
+    // sum in j order; a dropped or empty slot (-2) adds nothing
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (!(row[j] >= 0 && row[j] < A)) continue;
+#pragma unroll
+      for (int u = 0; u < CPT; ++u) Vec8<T>::load_acc(&q[j][u], wt[j], acc[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < CPT; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nchunk) Vec8<T>::store(out + t * d + static_cast<int64_t>(c) * E, acc[u]);
+    }
+    return;
+  }
   for (int j = 0; j < k; ++j) {
     const int64_t row = inv_perm[t * k + j];
     const float w = topk_w[t * k + j];

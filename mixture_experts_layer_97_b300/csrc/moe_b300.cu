@@ -295,7 +295,6 @@ EncodeTiledFn encode_fn() {
 
 // Tiling of the bf16 grouped GEMMs (moe_set_ffn_tiling), process wide.
 std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
-constexpr int kAutoPairMaxRowsPerExpert = 512;
 
 // bf16 matrix [rows, cols] row-major; box = box_rows x box_cols columns with the
 // swizzle whose span is one box row (box_cols * 2 bytes: 128 or 64).
@@ -415,15 +414,10 @@ moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* 
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
-  // "pairs" runs token tiles on SM pairs, "tokens" on single SMs; auto takes
-  // pairs while experts average fewer than 512 rows (weight streaming
-  // dominates there; measured 3.5 % faster on 256 rows per expert, ~1 %
-  // slower on 1024)
-  const int mode = g_ffn_tiling.load(std::memory_order_relaxed);
-  const bool pairs = mode == MOE_TILING_PAIRS ||
-                     (mode == MOE_TILING_AUTO && n_assign(s) < static_cast<int64_t>(kAutoPairMaxRowsPerExpert) * s->N);
-  if (pairs) return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
-  return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
+  // auto and "pairs" run token tiles on SM pairs, "tokens" on single SMs
+  if (g_ffn_tiling.load(std::memory_order_relaxed) == MOE_TILING_TOKENS)
+    return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
+  return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
 }
 
 // Process-wide choice between the two tensor-core tilings (moe_set_ffn_tiling).
@@ -488,15 +482,22 @@ moe_status combine_impl(const moe_shape* s, const void* y_perm, const int32_t* i
   const int nchunk = s->d / (s->dtype == MOE_BF16 ? 8 : 4);
   const int64_t warps = s->T * combine_groups<CPT>(nchunk);
   const int64_t grid = (warps + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
-  if (s->dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16, CPT><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
-        static_cast<__nv_bfloat16*>(out));
-  else
-    combine_kernel<float, CPT><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
-        static_cast<const float*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
-        static_cast<float*>(out));
-  return launched();
+  auto go = [&](auto kmax) {
+    constexpr int KMAX = decltype(kmax)::value;
+    if (s->dtype == MOE_BF16)
+      combine_kernel<__nv_bfloat16, CPT, KMAX><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
+          static_cast<__nv_bfloat16*>(out));
+    else
+      combine_kernel<float, CPT, KMAX><<<static_cast<unsigned>(grid), kCombineThreads, 0, st>>>(
+          static_cast<const float*>(y_perm), inv_perm, topk_w, s->T, s->d, s->k, n_assign(s),
+          static_cast<float*>(out));
+    return launched();
+  };
+  if (s->k <= 2) return go(std::integral_constant<int, 2>{});
+  if (s->k <= 4) return go(std::integral_constant<int, 4>{});
+  if (s->k <= 8) return go(std::integral_constant<int, 8>{});
+  return go(std::integral_constant<int, 0>{});
 }
 
 moe_status forward_impl(const moe_shape* s, const void* x, const float* wg, const float* bias, const void* w_gate,

@@ -72,6 +72,21 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
   const int n = valid ? 4 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
+// Two independent fp32 FMA chains in one instruction: d.lo = fma(a.lo, b.lo,
+// d.lo), d.hi = fma(a.hi, b.hi, d.hi), each rounded to nearest like fmaf, so
+// a logit's chain is the same as with scalar FMAs.
+__device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long a, unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ unsigned long long splat2(float v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
@@ -149,11 +164,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
     }
   };
 
+  // Accumulators: with two or more experts per thread, pairs of neighbouring
+  // experts share one packed register pair and one f32x2 FMA.
+  constexpr bool PACKED = EPT >= 2;
+  constexpr int EP2 = PACKED ? EPT / 2 : 1;
   float acc[TPT][EPT];
+  unsigned long long acc2[TPT][EP2];
 #pragma unroll
-  for (int i = 0; i < TPT; ++i)
+  for (int i = 0; i < TPT; ++i) {
 #pragma unroll
     for (int j = 0; j < EPT; ++j) acc[i][j] = 0.f;
+#pragma unroll
+    for (int p = 0; p < EP2; ++p) acc2[i][p] = 0ull;
+  }
 
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) {
@@ -176,29 +199,45 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
         load_x8(reinterpret_cast<const TX*>(xst + (ty * TPT + i) * C::XROW) + k8, xv[i]);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        float wv[EPT];
         const float* wr = wst + (k8 + u) * NP + V * tx;
+        if constexpr (PACKED) {
+          unsigned long long wp[EP2];   // (expert 2p, expert 2p + 1) of this thread
 #pragma unroll
-        for (int m = 0; m < EPT / V; ++m) {
-          if (V == 4) {
-            const float4 q = *reinterpret_cast<const float4*>(wr + V * EG * m);
-            wv[4 * m] = q.x; wv[4 * m + 1] = q.y; wv[4 * m + 2] = q.z; wv[4 * m + 3] = q.w;
-          } else if (V == 2) {
-            const float2 q = *reinterpret_cast<const float2*>(wr + V * EG * m);
-            wv[2 * m] = q.x; wv[2 * m + 1] = q.y;
-          } else {
-            wv[m] = wr[EG * m];
+          for (int m = 0; m < EPT / V; ++m) {
+            if constexpr (V == 4) {
+              const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(wr + V * EG * m);
+              wp[2 * m] = q.x;
+              wp[2 * m + 1] = q.y;
+            } else {
+              wp[m] = *reinterpret_cast<const unsigned long long*>(wr + V * EG * m);
+            }
           }
+#pragma unroll
+          for (int i = 0; i < TPT; ++i) {
+            const unsigned long long xx = splat2(xv[i][u]);
+#pragma unroll
+            for (int p = 0; p < EP2; ++p) ffma2(acc2[i][p], xx, wp[p]);
+          }
+        } else {
+          float wv[EPT];
+#pragma unroll
+          for (int m = 0; m < EPT; ++m) wv[m] = wr[EG * m];
+#pragma unroll
+          for (int i = 0; i < TPT; ++i)
+#pragma unroll
+            for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xv[i][u], wv[j], acc[i][j]);
         }
-#pragma unroll
-        for (int i = 0; i < TPT; ++i)
-#pragma unroll
-          for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xv[i][u], wv[j], acc[i][j]);
       }
     }
   }
   cp_async_wait<0>();
   __syncthreads();
+  if constexpr (PACKED) {
+#pragma unroll
+    for (int i = 0; i < TPT; ++i)
+#pragma unroll
+      for (int p = 0; p < EP2; ++p) unpack2(acc2[i][p], acc[i][2 * p], acc[i][2 * p + 1]);
+  }
 
   // logits (+ bias, unless it only chooses) -> lg[token][n]; padded experts get -inf
 #pragma unroll

@@ -473,6 +473,7 @@ def main():
             e2e.update({"value": job_throughput(w.T, world, p_ms), "ms_per_step": p_ms,
                         "mode": ("pipelined: moe_forward_hostio_pipelined over consecutive steps; every step "
                                  "copies its x in and its output out, overlapping the neighbouring steps' layer"),
+                        "l2": "no flush between pipelined steps: the expert weights every step reads exceed L2",
                         "serial_value": job_throughput(w.T, world, e_ms), "serial_ms_per_step": e_ms})
 
     if rank != 0:

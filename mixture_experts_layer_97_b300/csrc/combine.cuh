@@ -105,26 +105,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __res
 #pragma unroll
       for (int u = 0; u < CPT; ++u) Vec8<T>::load_acc(&q[j][u], wt[j], acc[u]);
     }
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int64_t row = inv_perm[t * k + j];
+      const float w = topk_w[t * k + j];
+      if (row == -2) continue;   // dropped by the expert capacity: adds nothing
+      if (row < 0 || row >= A) {
+        if (c0 == 0) record_error(MOE_ERR_CORRUPT);
+        continue;
+      }
+      const T* yr = y_perm + row * d;
 #pragma unroll
-    for (int u = 0; u < CPT; ++u) {
-      const int c = c0 + 32 * u;
-      if (c < nchunk) Vec8<T>::store(out + t * d + static_cast<int64_t>(c) * E, acc[u]);
-    }
-    return;
-  }
-  for (int j = 0; j < k; ++j) {
-    const int64_t row = inv_perm[t * k + j];
-    const float w = topk_w[t * k + j];
-    if (row == -2) continue;   // dropped by the expert capacity: adds nothing
-    if (row < 0 || row >= A) {
-      if (c0 == 0) record_error(MOE_ERR_CORRUPT);
-      continue;
-    }
-    const T* yr = y_perm + row * d;
-#pragma unroll
-    for (int u = 0; u < CPT; ++u) {
-      const int c = c0 + 32 * u;
-      if (c < nchunk) Vec8<T>::load_acc(yr + static_cast<int64_t>(c) * E, w, acc[u]);
+      for (int u = 0; u < CPT; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < nchunk) Vec8<T>::load_acc(yr + static_cast<int64_t>(c) * E, w, acc[u]);
+      }
     }
   }
 #pragma unroll

@@ -378,15 +378,38 @@ def main():
     if st != B.MOE_OK:
         raise RuntimeError(f"device error during warm-up: {B.status_string(st)}")
 
+    # The step captured once as a CUDA graph (the library only queues work on the caller's stream), so
+    # that a replayed step has no host launch gaps between its kernels.
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                step()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+    except RuntimeError:
+        graph = None
+
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    gevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
-        for i in range(args.steps):
+        for i in range(args.steps):            # eager steps, one event pair per stage
             flush_l2()                         # L2 flush between timed steps (outside the events)
             step(evs[i])
+        if graph is not None:
+            for i in range(args.steps):        # replayed steps, one event pair per step
+                flush_l2()
+                gevs[i][0].record(stream)
+                graph.replay()
+                gevs[i][1].record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
     if dist:
@@ -395,9 +418,10 @@ def main():
     if st != B.MOE_OK:
         raise RuntimeError(f"device error during timing: {B.status_string(st)}")
     stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
-    step_ms = float(stage.sum(1).mean())
-    ffn_ms = float(stage[:, 2].mean())
-    step_ms = max_over_ranks(step_ms, dist, "cuda")
+    eager_ms = float(np.median(stage.sum(1)))
+    ffn_ms = float(np.median(stage[:, 2]))
+    graph_ms = float(np.median([a.elapsed_time(b) for a, b in gevs])) if graph is not None else None
+    step_ms = max_over_ranks(graph_ms if graph_ms is not None else eager_ms, dist, "cuda")
 
     # end to end through the public host-buffer entry point
     e2e = None
@@ -527,16 +551,21 @@ def main():
                    "gate": "fp32", "ffn_tiling": args.ffn_tiling, "capacity_factor": cf,
                    "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write, then 2 x 126 MB read of another buffer); expert weights also exceed L2"},
+        "timing": ("median of CUDA-graph replays of the whole step (ms_per_step); stage_ms are medians of "
+                   "eager steps with an event pair per stage" if graph_ms is not None else
+                   "median of eager steps (graph capture unavailable)"),
+        "ms_per_step_eager": eager_ms,
         "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
-        "stage_ms": {"route": float(stage[:, 0].mean()), "permute": float(stage[:, 1].mean()),
-                     "grouped_ffn": ffn_ms, "combine": float(stage[:, 3].mean())},
+        "stage_ms": {"route": float(np.median(stage[:, 0])), "permute": float(np.median(stage[:, 1])),
+                     "grouped_ffn": ffn_ms, "combine": float(np.median(stage[:, 3]))},
         "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()),
         "dropped_assignments": int(dropped.item()) if cf is not None else 0,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         # token choice: route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1;
         # expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
-        "gpu_launches": (6 if ec else 8) * args.steps,
+        # (eager steps, then as many graph-replayed steps)
+        "gpu_launches": (6 if ec else 8) * args.steps * (2 if graph_ms is not None else 1),
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),
     }

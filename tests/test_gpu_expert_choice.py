@@ -201,3 +201,28 @@ def test_forward_expert_choice_worked_example_shapes():
     ref = ec_reference(inp, g, tokens)
     got = host_f64(out[torch.from_numpy(tokens).cuda()])
     assert rel_err(got, ref) <= tol(w.dtype)
+
+
+def test_route_expert_choice_empty_batch():
+    s = B.shape(0, 128, 8, 2, 64, "swiglu", "bf16")
+    counts, offsets = new((8,), "i32", fill=-1), new((9,), "i32", fill=-1)
+    wg = torch.zeros((128, 8), dtype=torch.float32, device="cuda")
+    B.route_expert_choice(s, 0, None, wg, None, None, None, counts, offsets, None, None)
+    assert B.get_error() == B.MOE_OK
+    assert counts.cpu().tolist() == [0] * 8 and offsets.cpu().tolist() == [0] * 9
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gather_rows_matches_indexing(dtype):
+    """moe_gather_rows with expert-choice tables: row r of x_perm is x[perm[r]];
+    slots marked -2 are skipped."""
+    w, C = ROUTE_CASES[1][0], 31
+    if dtype == "f32":
+        w = S.Workload("ec-gather-f32", T=500, d=64, N=16, k=2, F=64, act="swiglu", dtype="f32", seed=78)
+    inp = Inputs(w, host_weights=False)
+    g = gpu_route_ec(inp, C)
+    rows = w.N * C
+    xp = new((rows, w.d), dtype, fill=0)
+    B.gather_rows(inp.shape, torch.from_numpy(g["inv"]).cuda(), w.N, rows, inp.x, xp)
+    assert B.get_error() == B.MOE_OK
+    assert torch.equal(xp, inp.x[torch.from_numpy(g["perm"]).long().cuda()])

@@ -401,11 +401,12 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
-        for i in range(args.steps):            # eager steps, one event pair per stage
+        for i in range(args.steps):
+            # an eager step (one event pair per stage) and a replayed step (one pair per step) in turn,
+            # so both see the same clocks and power state
             flush_l2()                         # L2 flush between timed steps (outside the events)
             step(evs[i])
-        if graph is not None:
-            for i in range(args.steps):        # replayed steps, one event pair per step
+            if graph is not None:
                 flush_l2()
                 gevs[i][0].record(stream)
                 graph.replay()
@@ -564,7 +565,7 @@ def main():
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         # token choice: route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1;
         # expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
-        # (eager steps, then as many graph-replayed steps)
+        # (eager steps and as many graph-replayed steps, interleaved)
         "gpu_launches": (6 if ec else 8) * args.steps * (2 if graph_ms is not None else 1),
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),

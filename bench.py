@@ -349,26 +349,35 @@ def main():
         flush_clean.max()
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        if ev: ev[0].record(stream)
+    def stage_route():
         if ec:
             B.route_expert_choice(s, C, x, wg, bias, probs, perm, counts, offsets, inv_ec, w_ec)
         else:
             B.route(s, x, wg, bias, idx, tw)
-        if ev: ev[1].record(stream)
+
+    def stage_permute():
         if ec:
             B.gather_rows(s, inv_ec, w.N, A, x, xp)
         elif cf is None:
             B.permute(s, idx, x, counts, offsets, perm, inv, xp, ws)
         else:
             B.permute_capacity(s, idx, x, cf, counts, offsets, perm, inv, xp, ws, dropped=dropped)
-        if ev: ev[2].record(stream)
+
+    def stage_ffn():
         B.grouped_ffn(s_rows, xp, offsets, WG, WU, WD, yp, ws)
-        if ev: ev[3].record(stream)
+
+    def stage_combine():
         if ec:
             B.combine(s_slots, yp, inv_ec, w_ec, out)
         else:
             B.combine(s, yp, inv, tw, out)
+
+    stages = [stage_route, stage_permute, stage_ffn, stage_combine]
+
+    def step(ev=None):
+        for j, fn in enumerate(stages):
+            if ev: ev[j].record(stream)
+            fn()
         if ev: ev[4].record(stream)
 
     for _ in range(args.warmup):
@@ -378,39 +387,37 @@ def main():
     if st != B.MOE_OK:
         raise RuntimeError(f"device error during warm-up: {B.status_string(st)}")
 
-    # The step captured once as a CUDA graph (the library only queues work on the caller's stream), so
-    # that a replayed step has no host launch gaps between its kernels.
-    graph = None
+    # Each stage captured once as a CUDA graph (the library only queues work on the caller's stream)
+    # and replayed between event pairs: a stage's own launches (four for the grouping) run without
+    # host gaps, and the events still give the per-stage breakdown.
+    graphs = None
     try:
-        graph = torch.cuda.CUDAGraph()
+        graphs = []
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(graph, stream=cap):
-                step()
+        for fn in stages:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    fn()
+            graphs.append(g)
         torch.cuda.synchronize()
-        graph.replay()
+        for g in graphs:
+            g.replay()
         torch.cuda.synchronize()
+        stages = [g.replay for g in graphs]
     except RuntimeError:
-        graph = None
+        graphs = None
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
-    gevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
         for i in range(args.steps):
-            # an eager step (one event pair per stage) and a replayed step (one pair per step) in turn,
-            # so both see the same clocks and power state
             flush_l2()                         # L2 flush between timed steps (outside the events)
             step(evs[i])
-            if graph is not None:
-                flush_l2()
-                gevs[i][0].record(stream)
-                graph.replay()
-                gevs[i][1].record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
     if dist:
@@ -419,10 +426,9 @@ def main():
     if st != B.MOE_OK:
         raise RuntimeError(f"device error during timing: {B.status_string(st)}")
     stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
-    eager_ms = float(np.median(stage.sum(1)))
+    per_step = np.array([e[0].elapsed_time(e[4]) for e in evs])
     ffn_ms = float(np.median(stage[:, 2]))
-    graph_ms = float(np.median([a.elapsed_time(b) for a, b in gevs])) if graph is not None else None
-    step_ms = max_over_ranks(graph_ms if graph_ms is not None else eager_ms, dist, "cuda")
+    step_ms = max_over_ranks(float(np.median(per_step)), dist, "cuda")
 
     # end to end through the public host-buffer entry point
     e2e = None
@@ -552,10 +558,8 @@ def main():
                    "gate": "fp32", "ffn_tiling": args.ffn_tiling, "capacity_factor": cf,
                    "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write, then 2 x 126 MB read of another buffer); expert weights also exceed L2"},
-        "timing": ("median of CUDA-graph replays of the whole step (ms_per_step); stage_ms are medians of "
-                   "eager steps with an event pair per stage" if graph_ms is not None else
-                   "median of eager steps (graph capture unavailable)"),
-        "ms_per_step_eager": eager_ms,
+        "timing": ("median over steps; every stage is a CUDA-graph replay between CUDA events on the stream"
+                   if graphs is not None else "median over steps of eager stage calls between CUDA events"),
         "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
         "stage_ms": {"route": float(np.median(stage[:, 0])), "permute": float(np.median(stage[:, 1])),
@@ -565,8 +569,7 @@ def main():
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         # token choice: route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1;
         # expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
-        # (eager steps and as many graph-replayed steps, interleaved)
-        "gpu_launches": (6 if ec else 8) * args.steps * (2 if graph_ms is not None else 1),
+        "gpu_launches": (6 if ec else 8) * args.steps,
         "clocks": clocks,
         "kernel_source": kernel_source_hash(),
     }

@@ -147,3 +147,36 @@ def test_pipelined_hostio_checks(L):
     assert st == B.MOE_ERR_INVALID_ARG          # slot must be 0 or 1
     st = L.moe_forward_hostio_pipelined(ctypes.byref(s), p, p, None, p, p, p, p, p, need - 1, 0, None, None, None)
     assert st == B.MOE_ERR_WORKSPACE
+
+
+def test_header_compiles_as_c99_and_links(L, tmp_path):
+    """The boundary is plain C: a C99 program that includes only include/moe.h
+    builds against libmoe_b300.so and calls the host-only entry points."""
+    src = tmp_path / "use_moe.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe.h"
+int main(void) {
+    moe_shape s = {4096, 4096, 8, 2, 14336, MOE_SWIGLU, MOE_BF16};
+    moe_shape bad = s;
+    bad.k = 9;
+    if (moe_version() < 100) return 1;
+    if (moe_check_shape(&s) != MOE_OK) return 2;
+    if (moe_check_shape(&bad) != MOE_ERR_INVALID_ARG) return 3;
+    if (moe_workspace_size(&s) == 0 || moe_workspace_size(&bad) != 0) return 4;
+    if (strcmp(moe_status_string(MOE_OK), "ok") != 0) return 5;
+    if (moe_route(&bad, NULL, NULL, NULL, NULL, NULL, NULL) != MOE_ERR_INVALID_ARG) return 6;
+    printf("%zu\n", moe_forward_hostio_pipelined_workspace_size(&s));
+    return 0;
+}
+""")
+    exe = tmp_path / "use_moe"
+    libdir = os.path.dirname(B.LIB_PATH)
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                           "-L", libdir, "-l:libmoe_b300.so", f"-Wl,-rpath,{libdir}", "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out
+    assert int(out.stdout.strip()) == B.hostio_pipelined_workspace_size(B.shape(4096, 4096, 8, 2, 14336, "swiglu",
+                                                                                 "bf16"))

@@ -57,8 +57,9 @@ __host__ __device__ inline int combine_groups(int nchunk) { return (nchunk + 32 
 
 // KMAX > 0: k <= KMAX, and the k (row, weight) pairs and then all k rows'
 // chunks are loaded before any is summed, so a lane has k * CPT row loads in
-// flight; KMAX = 0: any k, one row after the other (the expert-choice path,
-// where k is the number of experts and most slots are empty).
+// flight; KMAX = 0: any k, live slots found by a warp ballot and summed one
+// row after the other (the expert-choice path, where k is the number of
+// experts and most slots are empty).
 template <typename T, int CPT, int KMAX>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __restrict__ y_perm,
                                                                   const int32_t* __restrict__ inv_perm,
@@ -106,19 +107,27 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const T* __res
       for (int u = 0; u < CPT; ++u) Vec8<T>::load_acc(&q[j][u], wt[j], acc[u]);
     }
   } else {
-    for (int j = 0; j < k; ++j) {
-      const int64_t row = inv_perm[t * k + j];
-      const float w = topk_w[t * k + j];
-      if (row == -2) continue;   // dropped by the expert capacity: adds nothing
-      if (row < 0 || row >= A) {
-        if (c0 == 0) record_error(MOE_ERR_CORRUPT);
-        continue;
-      }
-      const T* yr = y_perm + row * d;
+    // many slots, few of them live (expert choice: k = N): each lane reads one
+    // slot, a ballot lists the live ones, and the warp sums their rows in slot order
+    const bool first_group = (gw % G) == 0;
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      const int j = j0 + lane;
+      const int64_t r = j < k ? inv_perm[t * k + j] : -2;
+      const float wj = j < k ? topk_w[t * k + j] : 0.f;
+      const bool live = r >= 0 && r < A;
+      if (r != -2 && !live && first_group) record_error(MOE_ERR_CORRUPT);
+      unsigned m = __ballot_sync(0xffffffffu, live);
+      while (m != 0u) {
+        const int b = __ffs(m) - 1;
+        m &= m - 1u;
+        const int64_t row = __shfl_sync(0xffffffffu, r, b);
+        const float w = __shfl_sync(0xffffffffu, wj, b);
+        const T* yr = y_perm + row * d;
 #pragma unroll
-      for (int u = 0; u < CPT; ++u) {
-        const int c = c0 + 32 * u;
-        if (c < nchunk) Vec8<T>::load_acc(yr + static_cast<int64_t>(c) * E, w, acc[u]);
+        for (int u = 0; u < CPT; ++u) {
+          const int c = c0 + 32 * u;
+          if (c < nchunk) Vec8<T>::load_acc(yr + static_cast<int64_t>(c) * E, w, acc[u]);
+        }
       }
     }
   }

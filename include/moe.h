@@ -283,7 +283,8 @@ moe_status moe_forward_hostio(const moe_shape *s, const void *x_host, const floa
  * stay unchanged until h2d_stream has passed the call. Device inputs
  * (weights, w_g, bias) must not change while calls are in flight. The
  * library creates eight events per device on first use (kept until the
- * process exits). ws: moe_forward_hostio_pipelined_workspace_size(s) bytes.
+ * process exits); they order the two slots, so one such pipeline runs per
+ * device at a time. ws: moe_forward_hostio_pipelined_workspace_size(s) bytes.
  * The pages name no such entry point: it exists so that host<->device copies
  * of consecutive batches hide behind the layer.
  */

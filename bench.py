@@ -514,6 +514,22 @@ def main():
 
     P = peaks()
     cnt = counts.cpu().numpy()
+    # routing health of the batch, from the library's own statistics (moe_route_ex), outside the timing
+    routing_stats = None
+    if not ec:
+        try:
+            st_buf = torch.empty(B.load_stats_len(w.N), dtype=torch.float32, device="cuda")
+            idx2 = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+            tw2 = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+            B.route_ex(s, x, wg, bias, idx2, tw2, load_stats=st_buf, ws=B.workspace(B.route_ex_workspace_size(s)))
+            if B.get_error() == B.MOE_OK:
+                u = B.unpack_load_stats(st_buf, w.N)
+                routing_stats = {"balance_N_sum_fP": u["balance"], "activation_entropy_bits": u["entropy_bits"],
+                                 "entropy_max_bits": float(np.log2(w.N)), "mean_top1_probability": u["top1"],
+                                 "expert_rows": {"min": int(cnt.min()), "median": float(np.median(cnt)),
+                                                 "max": int(cnt.max()), "empty": int((cnt == 0).sum())}}
+        except Exception:                      # a report extra: never let it stop the benchmark line
+            routing_stats = None
     rows = int(cnt.sum())                      # rows the grouped FFN computed (A unless a capacity dropped some)
     up_f, down_f = acc.up_flops(rows, w.d, w.F, w.act), acc.down_flops(rows, w.d, w.F)
     ffn_flops = up_f + down_f
@@ -564,7 +580,7 @@ def main():
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
         "stage_ms": {"route": float(np.median(stage[:, 0])), "permute": float(np.median(stage[:, 1])),
                      "grouped_ffn": ffn_ms, "combine": float(np.median(stage[:, 3]))},
-        "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()),
+        "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()), "routing_stats": routing_stats,
         "dropped_assignments": int(dropped.item()) if cf is not None else 0,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         # token choice: route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1;

@@ -4,6 +4,10 @@ Argument marshalling only: tensors become device pointers, the current torch
 stream becomes the cudaStream_t, a non-OK status becomes ``MoEError``. Every
 step of the layer runs in the library's kernels. There is no CPU fallback:
 if the library is missing or a tensor is not on a CUDA device, calls raise.
+
+Each function ``name`` wraps the C entry point ``moe_name`` with the same
+arguments in the same order (a workspace tensor supplies both the pointer and
+its byte size); the header documents meaning, layouts and errors.
 """
 from __future__ import annotations
 

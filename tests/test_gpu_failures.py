@@ -30,8 +30,9 @@ def test_bounded_wait_times_out_and_context_survives():
 
 def test_corrupt_routing_in_forward_is_reported_not_faulted():
     """An out-of-range expert index fed to the staged path: the permute records
-    MOE_ERR_CORRUPT, the GEMMs see offsets that do not add up and do nothing,
-    the combine skips rows it cannot trust. Nothing reads out of bounds."""
+    MOE_ERR_CORRUPT and places only the valid assignments (a prefix of the
+    rows, which the GEMMs accept), and the combine skips the slot it cannot
+    trust. Nothing reads out of bounds."""
     w = S.Workload("corrupt", T=100, d=128, N=8, k=2, F=128, act="swiglu", dtype="bf16", seed=6)
     inp = Inputs(w)
     s = inp.shape

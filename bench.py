@@ -36,7 +36,7 @@ from mixture_experts_layer_97_b300 import accounting as acc  # noqa: E402
 DEFAULT_WORKLOAD = "worked-example-n64-f16384-gelu"
 L2_BYTES = 126 * 1024 * 1024
 NOMINAL_BF16_TFLOPS = 2250.0
-NOMINAL_HBM_GBS = 7700.0
+NOMINAL_HBM_GBS = 8000.0   # nominal HBM3e bandwidth of a B300, ~8 TB/s (context fraction only)
 
 
 def peaks():
@@ -557,7 +557,7 @@ def main():
                 "algorithmic_bytes_per_call": wbytes}
     fwd_bytes = acc.decode_forward_bytes(cnt, w.T, w.d, w.N, w.k, w.F, w.act, w.esize)
     roof["forward_frac_hbm"] = fwd_bytes / (step_ms * 1e-3) / 1e9 / P["hbm"]
-    # context only: against the nominal 2.25 PFLOP/s bf16 dense and 7.7 TB/s HBM3e of the part
+    # context only: against the nominal 2.25 PFLOP/s bf16 dense and ~8 TB/s HBM3e of the part
     roof["frac_of_nominal"] = (tflops / NOMINAL_BF16_TFLOPS) if tensor_bound else (gbs / NOMINAL_HBM_GBS)
 
     cpu = None

@@ -133,7 +133,9 @@ moe_status moe_permute(const moe_shape *s, const int32_t *topk_idx, const void *
  * rows offsets[N] .. A-1 are ignored), y_perm [A,d].
  * bf16: tcgen05 tensor cores, fp32 accumulation in tensor memory, h rounded
  * to bf16; f32: fp32 CUDA-core GEMM. ws: moe_grouped_ffn_workspace_size(s)
- * bytes (holds h). Offsets that are not a monotone partition of a prefix
+ * bytes; on return its first A*F elements (dtype of s) hold h [A, F] in the
+ * rows of x_perm (rows past offsets[N] unwritten). Offsets that are not a
+ * monotone partition of a prefix
  * [0, offsets[N]) of the A rows record MOE_ERR_CORRUPT and the GEMMs do
  * nothing.
  */
@@ -196,6 +198,10 @@ moe_status moe_forward_capacity(const moe_shape *s, double capacity_factor, cons
  *   load_stats      device, MOE_LOAD_STATS_LEN(N) floats, or NULL (see
  *                   moe_route_ex; statistics of the routing, before any drop)
  *   dropped         device int32, or NULL: assignments dropped by the capacity
+ *   use_tiling      nonzero: this call's grouped GEMMs use ffn_tiling (a
+ *                   moe_tiling value) instead of the process-wide setting of
+ *                   moe_set_ffn_tiling, so callers in one process that want
+ *                   different tilings do not share a global
  * opt == NULL is the plain moe_forward. ws: moe_workspace_size(s) bytes.
  */
 typedef struct {
@@ -204,6 +210,8 @@ typedef struct {
     double capacity_factor;
     float *load_stats;
     int32_t *dropped;
+    int32_t use_tiling;
+    int32_t ffn_tiling;
 } moe_options;
 moe_status moe_forward_ex(const moe_shape *s, const moe_options *opt, const void *x, const float *w_g,
                           const float *bias, const void *w_gate, const void *w_up,

@@ -40,7 +40,8 @@ class MoeShape(ctypes.Structure):
 
 class MoeOptions(ctypes.Structure):
     _fields_ = [("bias_mode", ctypes.c_int32), ("use_capacity", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
-                ("load_stats", ctypes.c_void_p), ("dropped", ctypes.c_void_p)]
+                ("load_stats", ctypes.c_void_p), ("dropped", ctypes.c_void_p), ("use_tiling", ctypes.c_int32),
+                ("ffn_tiling", ctypes.c_int32)]
 
 
 SP = ctypes.POINTER(MoeShape)
@@ -204,11 +205,14 @@ def unpack_load_stats(t, N: int) -> dict:
 
 
 def forward_ex(s, x, w_g, bias, w_gate, w_up, w_down, out, ws, bias_mode="logits", capacity_factor=None,
-               load_stats=None, dropped=None, topk_idx=None, topk_w=None, counts=None, stream=None):
+               load_stats=None, dropped=None, topk_idx=None, topk_w=None, counts=None, ffn_tiling=None,
+               stream=None):
+    """ffn_tiling: None (the process-wide setting) or a key of TILING for this call only."""
     o = MoeOptions(BIAS_MODES[bias_mode], 0 if capacity_factor is None else 1,
                    0.0 if capacity_factor is None else float(capacity_factor),
                    None if load_stats is None else _ptr(load_stats).value,
-                   None if dropped is None else _ptr(dropped).value)
+                   None if dropped is None else _ptr(dropped).value,
+                   0 if ffn_tiling is None else 1, 0 if ffn_tiling is None else TILING[ffn_tiling])
     _check(lib().moe_forward_ex(ctypes.byref(s), ctypes.byref(o), _ptr(x), _ptr(w_g), _ptr(bias), _ptr(w_gate),
                                 _ptr(w_up), _ptr(w_down), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(counts),
                                 _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_ex")

@@ -72,6 +72,7 @@ struct FwdOpts {
   long long capacity = kNoCapacity;    // rows an expert keeps
   int32_t* dropped = nullptr;          // device [1]: dropped assignments
   float* load_stats = nullptr;         // device [2N + 3]: routing statistics
+  int tiling = -1;                     // grouped-GEMM tiling of this call; -1: the process-wide setting
 };
 
 struct FwdBufs {
@@ -136,17 +137,20 @@ moe_status shape_status(const moe_shape* s) {
 
 bool ptr_ok(const void* p, bool needed) { return needed ? (p != nullptr && aligned16(p)) : (p == nullptr || aligned16(p)); }
 
+// SM count of the current device, looked up once per device. Host threads may
+// race on the first lookup: each slot is an atomic, and every racer stores the
+// same value.
 int num_sms() {
-  static int cache[kMaxDevices] = {0};
+  static std::atomic<int> cache[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
   if (dev < 0 || dev >= kMaxDevices) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_acquire);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_release);
   }
-  return cache[dev];
+  return n;
 }
 
 moe_status launched() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -282,21 +286,29 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, resolved once per process (std::call_once:
+// safe when several host threads make their first call together).
 EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+  });
   return fn;
 }
 
-// Tiling of the bf16 grouped GEMMs (moe_set_ffn_tiling), process wide.
+// Tiling of the bf16 grouped GEMMs (moe_set_ffn_tiling), process wide; a
+// moe_forward_ex call can override it for itself (moe_options.use_tiling).
 std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
+
+bool tiling_valid(int mode) {
+  return mode == MOE_TILING_AUTO || mode == MOE_TILING_ROWS || mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS;
+}
 
 // bf16 matrix [rows, cols] row-major; box = box_rows x box_cols columns with the
 // swizzle whose span is one box row (box_cols * 2 bytes: 128 or 64).
@@ -415,22 +427,18 @@ moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* 
 
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
-                          const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+                          const int32_t* offsets, void* out, int ldo, cudaStream_t st, int mode) {
   // auto and "pairs" run token tiles on SM pairs, "tokens" on single SMs
-  if (g_ffn_tiling.load(std::memory_order_relaxed) == MOE_TILING_TOKENS)
+  if (mode == MOE_TILING_TOKENS)
     return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
   return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
 }
-
-// Process-wide choice between the two tensor-core tilings (moe_set_ffn_tiling).
-
 
 // K is the reduction length of the GEMM in question (d for the first, F for
 // the second). Token tiles pad less but keep one accumulator pair in TMEM, so
 // their epilogue is not overlapped with the next tile: they pay off when an
 // expert holds enough rows to fill tiles and K is long enough to hide it.
-bool use_token_tiles(const moe_shape* s, int K) {
-  const int mode = g_ffn_tiling.load(std::memory_order_relaxed);
+bool use_token_tiles(const moe_shape* s, int K, int mode) {
   if (mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS) return true;
   if (mode == MOE_TILING_ROWS) return false;
   return n_assign(s) >= static_cast<int64_t>(kAutoTokenTileMinRowsPerExpert) * s->N && K >= kAutoTokenTileMinK;
@@ -449,16 +457,21 @@ moe_status launch_simt(const moe_shape* s, const void* a, int K, const void* b0,
   return launched();
 }
 
+// tiling: a moe_tiling value for this call, or -1 for the process-wide setting
+// (moe_set_ffn_tiling), read once per call so both GEMMs see the same mode.
 moe_status ffn_impl(const moe_shape* s, const void* x_perm, const int32_t* offsets, const void* w_gate,
-                    const void* w_up, const void* w_down, void* y_perm, void* ws, cudaStream_t st) {
+                    const void* w_up, const void* w_down, void* y_perm, void* ws, cudaStream_t st,
+                    int tiling = -1) {
   if (n_assign(s) == 0) return MOE_OK;
   const int d = s->d, F = s->d_ff;
+  const int mode = tiling >= 0 ? tiling : g_ffn_tiling.load(std::memory_order_relaxed);
   void* h = ws;
   moe_status r;
   if (s->dtype == MOE_BF16) {
-    if (use_token_tiles(s, d))
-      r = (s->act == MOE_SWIGLU) ? launch_tc_swap<EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
-                                 : launch_tc_swap<EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
+    if (use_token_tiles(s, d, mode))
+      r = (s->act == MOE_SWIGLU)
+              ? launch_tc_swap<EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st, mode)
+              : launch_tc_swap<EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st, mode);
     else if (s->act == MOE_SWIGLU)
       r = (F % 128 == 0) ? launch_tc<256, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
                          : launch_tc<128, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st);
@@ -466,7 +479,8 @@ moe_status ffn_impl(const moe_shape* s, const void* x_perm, const int32_t* offse
       r = (F % 256 == 0) ? launch_tc<256, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st)
                          : launch_tc<128, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
     if (r != MOE_OK) return r;
-    if (use_token_tiles(s, F)) return launch_tc_swap<EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
+    if (use_token_tiles(s, F, mode))
+      return launch_tc_swap<EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st, mode);
     return (d % 256 == 0) ? launch_tc<256, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st)
                           : launch_tc<128, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
   }
@@ -512,7 +526,7 @@ moe_status forward_impl(const moe_shape* s, const void* x, const float* wg, cons
   if (r != MOE_OK) return r;
   r = permute_impl(s, idx, x, cnt, b.offsets, b.perm, b.inv_perm, b.x_perm, b.perm_ws, st, o.capacity, o.dropped);
   if (r != MOE_OK) return r;
-  r = ffn_impl(s, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st);
+  r = ffn_impl(s, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st, o.tiling);
   if (r != MOE_OK) return r;
   return combine_impl(s, b.y_perm, b.inv_perm, w, out, st);
 }
@@ -768,6 +782,8 @@ moe_status moe_forward_ex(const moe_shape* s, const moe_options* opt, const void
     if (opt->bias_mode != MOE_BIAS_LOGITS && opt->bias_mode != MOE_BIAS_SELECT) return MOE_ERR_INVALID_ARG;
     if (opt->use_capacity && !(opt->capacity_factor >= 0.0)) return MOE_ERR_INVALID_ARG;
     if (!ptr_ok(opt->load_stats, false) || !ptr_ok(opt->dropped, false)) return MOE_ERR_INVALID_ARG;
+    if (opt->use_tiling && !tiling_valid(opt->ffn_tiling)) return MOE_ERR_INVALID_ARG;
+    if (opt->use_tiling) o.tiling = opt->ffn_tiling;
     o.bias_select = opt->bias_mode == MOE_BIAS_SELECT ? 1 : 0;
     if (opt->use_capacity) o.capacity = capacity_rows(s, opt->capacity_factor);
     o.load_stats = opt->load_stats;
@@ -948,6 +964,24 @@ moe_status moe_forward_hostio_pipelined(const moe_shape* s, const void* x_host, 
 // device address comes from cudaGetSymbolAddress, looked up once per device.
 static __device__ __align__(256) int32_t g_permute_noalloc_scratch[MOE_PERMUTE_NOALLOC_SCRATCH_INTS];
 
+// The current device's address of the scratch array, looked up on the first
+// call on that device (with the device current) and cached under a mutex, so
+// host threads that make their first calls together are safe. The cache is not
+// refreshed after cudaDeviceReset: the library is not usable across a reset.
+static void* noalloc_scratch_address() {
+  static void* addr[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_permute_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
 moe_status moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, const void* x, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* x_perm, void* stream) {
   moe_status st = shape_status(s);
@@ -957,21 +991,14 @@ moe_status moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, cons
       !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, any))
     return MOE_ERR_INVALID_ARG;
   if (perm_chunks(s) * s->N > MOE_PERMUTE_NOALLOC_SCRATCH_INTS) return MOE_ERR_WORKSPACE;
-  static void* scratch_addr[kMaxDevices] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
-  if (scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_permute_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    scratch_addr[dev] = p;
-  }
-  return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, scratch_addr[dev],
+  void* scratch = noalloc_scratch_address();
+  if (scratch == nullptr) return MOE_ERR_CUDA;
+  return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, scratch,
                       static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_set_ffn_tiling(int mode) {
-  if (mode != MOE_TILING_AUTO && mode != MOE_TILING_ROWS && mode != MOE_TILING_TOKENS && mode != MOE_TILING_PAIRS)
-    return MOE_ERR_INVALID_ARG;
+  if (!tiling_valid(mode)) return MOE_ERR_INVALID_ARG;
   g_ffn_tiling.store(mode, std::memory_order_relaxed);
   return MOE_OK;
 }

@@ -26,7 +26,7 @@
  *        (gate, up, SiLU(gate)*up, down); s5.1 count -> prefix sum -> permute ->
  *        per-expert GEMM -> unpermute + weighted merge.
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings where the pages are silent or ambiguous, taken here:
  *   - the gate is computed in fp32 ([P3] s2.4 and s7 keep the gate in FP32
  *     and the experts in bf16). Its plainest fp32 evaluation is used: for
  *     each logit the sequential chain s <- fma(x_i, W_g[i,n], s) over

@@ -65,7 +65,10 @@ def new(shape, dtype, fill=None):
 class Inputs:
     """A workload's seeded inputs on the device (and its small pieces on host)."""
 
-    def __init__(self, w: S.Workload, host_weights: bool = True):
+    def __init__(self, w: S.Workload, host_weights: bool = True, on_expert=None):
+        """on_expert(e, (w_gate, w_up, w_down)), if given, is called with each
+        expert's host weights as they are uploaded (one pass over the weights
+        serves the device copy and the oracle)."""
         self.w = w
         self.x_h = S.x_all(w)
         self.wg_h = S.gate_weight(w)
@@ -85,6 +88,8 @@ class Inputs:
             self.w_down[e].copy_(dev(c))
             if self.host is not None:
                 self.host[e] = (a, b, c)
+            if on_expert is not None:
+                on_expert(e, (a, b, c))
         torch.cuda.synchronize()
 
     def expert(self, e):

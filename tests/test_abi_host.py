@@ -154,6 +154,7 @@ def test_header_compiles_as_c99_and_links(L, tmp_path):
     builds against libmoe_b300.so and calls the host-only entry points."""
     src = tmp_path / "use_moe.c"
     src.write_text(r"""
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 #include "moe.h"
@@ -167,7 +168,8 @@ int main(void) {
     if (moe_workspace_size(&s) == 0 || moe_workspace_size(&bad) != 0) return 4;
     if (strcmp(moe_status_string(MOE_OK), "ok") != 0) return 5;
     if (moe_route(&bad, NULL, NULL, NULL, NULL, NULL, NULL) != MOE_ERR_INVALID_ARG) return 6;
-    printf("%zu\n", moe_forward_hostio_pipelined_workspace_size(&s));
+    printf("%zu %zu %zu %zu\n", moe_forward_hostio_pipelined_workspace_size(&s), sizeof(moe_options),
+           offsetof(moe_options, use_tiling), offsetof(moe_options, ffn_tiling));
     return 0;
 }
 """)
@@ -178,5 +180,17 @@ int main(void) {
                            "-L", libdir, "-l:libmoe_b300.so", f"-Wl,-rpath,{libdir}", "-o", str(exe)])
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, out
-    assert int(out.stdout.strip()) == B.hostio_pipelined_workspace_size(B.shape(4096, 4096, 8, 2, 14336, "swiglu",
-                                                                                 "bf16"))
+    ws, size, off_use, off_tiling = (int(v) for v in out.stdout.split())
+    assert ws == B.hostio_pipelined_workspace_size(B.shape(4096, 4096, 8, 2, 14336, "swiglu", "bf16"))
+    # the binding's options struct has the header's layout
+    assert size == ctypes.sizeof(B.MoeOptions)
+    assert off_use == B.MoeOptions.use_tiling.offset and off_tiling == B.MoeOptions.ffn_tiling.offset
+
+
+def test_forward_ex_rejects_a_bad_per_call_tiling(L):
+    s = S()
+    p = ctypes.c_void_p(0x1000)
+    o = B.MoeOptions(0, 0, 0.0, None, None, 1, 7)
+    st = L.moe_forward_ex(ctypes.byref(s), ctypes.byref(o), p, p, None, p, p, p, p, None, None, None, p, 1 << 40,
+                          None)
+    assert st == B.MOE_ERR_INVALID_ARG

@@ -3,7 +3,9 @@
 Small workloads run the full oracle layer; the full-size workloads (in the
 launch configuration the benchmark times: route -> permute -> grouped FFN ->
 combine on one stream) check routing, counts and the permutation bit-exactly
-on every token and the outputs of sampled tokens against the oracle."""
+on every token, h and y_perm on a row set that holds every tile block of the
+grouped GEMMs, and the outputs of every token (decode, skewed batch) or of
+at least one token per expert (prefill, worked example)."""
 import numpy as np
 import pytest
 import torch
@@ -11,8 +13,8 @@ import torch
 import moe_synth as S
 import oracle
 from mixture_experts_layer_97_b300 import binding as B
-from tests.gpu_util import (Inputs, check_route, dev, host_f64, new, oracle_outputs_for_tokens, rel_err,
-                            run_forward, tol)
+from tests import tiles
+from tests.gpu_util import Inputs, check_route, dev, host_f64, new, rel_err, run_forward, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -144,38 +146,102 @@ def staged_forward(inp: Inputs):
     B.grouped_ffn(s, xp, offsets, inp.w_gate, inp.w_up, inp.w_down, yp, ws)
     B.combine(s, yp, inv, tw, out)
     assert B.get_error() == B.MOE_OK
-    return dict(idx=idx, tw=tw, counts=counts, offsets=offsets, perm=perm, inv=inv, xp=xp, yp=yp, out=out)
+    return dict(idx=idx, tw=tw, counts=counts, offsets=offsets, perm=perm, inv=inv, xp=xp, yp=yp, out=out, ws=ws)
 
 
 FULL = ["decode-t32-n64-k8", "prefill-n8-f14336", "zipf-skew-n128-k8", "worked-example-n64-f16384-gelu"]
+# every output row compared where the oracle finishes the whole batch in about a minute
+WHOLE_BATCH = {"decode-t32-n64-k8", "zipf-skew-n128-k8"}
+
+
+def _h_rows(ws: torch.Tensor, rows: np.ndarray, A: int, F: int) -> torch.Tensor:
+    """Rows of the hidden activations h [A, F] (bf16) that moe_grouped_ffn
+    leaves at the start of its workspace."""
+    h = ws[:A * F * 2].view(torch.bfloat16).view(A, F)
+    return h[torch.from_numpy(rows).cuda()]
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_forward_full_size(name):
+    """Full-size parity in the launch configuration the benchmark times.
+
+    - top-k indices, counts, offsets, perm and inv_perm: bit-exact on every token;
+    - x_perm: every row equals x[perm[row]];
+    - h and y_perm: element by element against the oracle's expert FFN on a
+      stratified row set that holds at least one row of every block of both
+      grouped-GEMM tilings (asserted from offsets), over all columns;
+    - out: every token on the decode and skewed batches (the whole y_perm
+      too), else at least one token per active expert.
+    """
     w = S.WORKLOADS[name]
-    inp = Inputs(w, host_weights=False)
+    x_h, wg_h, bias_h = S.x_all(w), S.gate_weight(w), S.gate_bias(w)
+    orc = oracle.route(x_h, wg_h, w.k, bias=bias_h)
+    pref = oracle.permute(orc["topk_idx"], w.N)
+    counts, offsets, perm = pref["counts"], pref["offsets"], pref["perm"]
+    strat = tiles.stratified_rows(offsets)
+    assert tiles.uncovered(counts, offsets, strat) == []
+    whole = name in WHOLE_BATCH
+    if whole:
+        out_tokens = np.arange(w.T)
+    else:   # the token of every active expert's first row, and of its last
+        firsts = [int(perm[offsets[e]]) for e in range(w.N) if counts[e] > 0]
+        lasts = [int(perm[offsets[e + 1] - 1]) for e in range(w.N) if counts[e] > 0]
+        out_tokens = np.unique(firsts + lasts)
+    out_rows = pref["inv_perm"].reshape(w.T, w.k)[out_tokens].reshape(-1)
+    y_rows = np.arange(w.A) if whole else np.union1d(strat, out_rows)
+
+    # oracle expert FFN on the needed rows, computed while the weights are uploaded
+    y_ref = np.zeros((w.A, w.d)) if whole else {}
+    h_ref = {}
+    strat_set = set(strat.tolist())
+
+    def on_expert(e, ws3):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        rows = y_rows[(y_rows >= lo) & (y_rows < hi)]
+        if rows.size == 0:
+            return
+        y, h = oracle.expert_rows(x_h[perm[rows]], ws3[0], ws3[1], ws3[2], w.act, want_h=True)
+        for i, r in enumerate(rows.tolist()):
+            y_ref[r] = y[i]
+            if r in strat_set:
+                h_ref[r] = h[i]
+
+    inp = Inputs(w, host_weights=False, on_expert=on_expert)
     r = staged_forward(inp)
-    # routing: bit-exact on every token
-    orc = oracle.route(inp.x_h, inp.wg_h, w.k, bias=inp.bias_h)
-    gi = r["idx"].cpu().numpy()
-    check_route(gi, r["tw"].cpu().numpy().astype(np.float64), orc)
-    # grouping: bit-exact
-    pref = oracle.permute(gi, w.N)
-    np.testing.assert_array_equal(r["counts"].cpu().numpy(), pref["counts"])
-    np.testing.assert_array_equal(r["offsets"].cpu().numpy(), pref["offsets"])
-    np.testing.assert_array_equal(r["perm"].cpu().numpy(), pref["perm"])
+
+    # routing and grouping: bit-exact
+    check_route(r["idx"].cpu().numpy(), r["tw"].cpu().numpy().astype(np.float64), orc)
+    np.testing.assert_array_equal(r["counts"].cpu().numpy(), counts)
+    np.testing.assert_array_equal(r["offsets"].cpu().numpy(), offsets)
+    np.testing.assert_array_equal(r["perm"].cpu().numpy(), perm)
     np.testing.assert_array_equal(r["inv"].cpu().numpy(), pref["inv_perm"])
-    rows = np.random.default_rng(0).choice(w.A, size=min(w.A, 512), replace=False)
-    assert torch.equal(r["xp"][torch.from_numpy(rows).cuda()],
-                       inp.x[torch.from_numpy(pref["perm"][rows]).long().cuda()])
-    # outputs of sampled tokens (every token for the decode batch)
-    n_s = w.T if w.T <= 32 else 24
-    tokens = np.sort(np.random.default_rng(1).choice(w.T, size=n_s, replace=False))
-    ref = oracle_outputs_for_tokens(inp, tokens, orc["topk_idx"], orc["topk_w"])
-    got = host_f64(r["out"][torch.from_numpy(tokens).cuda()])
-    err = rel_err(got, ref)
-    print(f"{name}: sampled-token max err / max|ref| = {err:.2e}")
-    assert err <= tol(w.dtype)
+    assert torch.equal(r["xp"], inp.x[r["perm"].long()])
+
+    # h and y_perm on the stratified rows (every block of both tilings)
+    hs = host_f64(_h_rows(r["ws"], strat, w.A, w.F))
+    h_err = rel_err(hs, np.stack([h_ref[q] for q in strat.tolist()]))
+    ys = host_f64(r["yp"][torch.from_numpy(strat).cuda()])
+    y_err = rel_err(ys, np.stack([y_ref[q] for q in strat.tolist()]))
+    # out on the chosen tokens
+    if whole:
+        y_full = y_ref
+    else:
+        y_full = np.zeros((w.A, w.d))
+        for q in out_rows.tolist():
+            y_full[q] = y_ref[q]
+    out_ref = oracle.combine(y_full, pref["inv_perm"], orc["topk_w"], tokens=out_tokens)
+    out_err = rel_err(host_f64(r["out"][torch.from_numpy(out_tokens).cuda()]), out_ref)
+    n_units = len(tiles.units(counts))
+    msg = (f"{name}: {len(strat)} stratified rows over {n_units} tile blocks of {int((counts > 0).sum())} experts, "
+           f"{len(out_tokens)} output tokens; max err / max|ref|: h {h_err:.2e}, y_perm {y_err:.2e}, out {out_err:.2e}")
+    if whole:
+        yall_err = rel_err(host_f64(r["yp"]), y_ref)
+        msg += f", whole y_perm {yall_err:.2e}"
+        assert yall_err <= tol(w.dtype)
+    print(msg)
+    assert h_err <= tol(w.dtype)
+    assert y_err <= tol(w.dtype)
+    assert out_err <= tol(w.dtype)
     # the one-call forward gives the same bits as the staged calls
     out1 = run_forward(inp)[0]
     assert torch.equal(out1, r["out"])

@@ -185,3 +185,23 @@ def test_forward_ex_without_options_is_the_plain_forward():
                  B.workspace(B.workspace_size(inp.shape)))
     assert B.get_error() == B.MOE_OK
     assert torch.equal(out, plain)
+
+
+def test_forward_ex_per_call_tiling_leaves_the_process_setting_alone():
+    """A per-call tiling gives, bit for bit, what the same tiling set process
+    wide gives, and does not change the process-wide setting."""
+    w = S.Workload("tiling-call", T=600, d=512, N=4, k=2, F=384, act="swiglu", dtype="bf16", seed=63)
+    inp = Inputs(w)
+    s = inp.shape
+    ws = B.workspace(B.workspace_size(s))
+    outs = {}
+    for mode in ("rows", "tokens", "pairs"):
+        B.set_ffn_tiling(mode)
+        outs[mode] = run_forward(inp)[0]
+    B.set_ffn_tiling("auto")
+    for mode in ("rows", "tokens", "pairs"):
+        out = new((w.T, w.d), w.dtype)
+        B.forward_ex(s, inp.x, inp.wg, inp.bias, inp.w_gate, inp.w_up, inp.w_down, out, ws, ffn_tiling=mode)
+        assert B.get_error() == B.MOE_OK
+        assert torch.equal(out, outs[mode]), mode
+        assert B.get_ffn_tiling() == "auto"

@@ -24,6 +24,7 @@ import subprocess
 import sys
 import threading
 import time
+from typing import Optional
 
 import numpy as np
 
@@ -249,46 +250,54 @@ def reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ fp32 FMA peak
+def fma_peak_tflops(torch, sms: int) -> dict:
+    """Measured fp32 FMA throughput of the CUDA cores (the route kernel's
+    roofline denominator): the committed microbenchmark libmoe_fma_peak.so,
+    scalar fma.rn.f32 and packed fma.rn.f32x2, best of 5 launches each timed
+    with CUDA events on the current stream."""
+    import ctypes
+    from mixture_experts_layer_97_b300 import build as build_mod
+    L = ctypes.CDLL(build_mod.build_fma_peak())
+    L.moe_fma_peak_flops.restype = ctypes.c_double
+    L.moe_fma_peak_flops.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.moe_fma_peak_launch.restype = ctypes.c_int
+    L.moe_fma_peak_launch.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_void_p]
+    blocks, threads, iters = sms * 8, 256, 4096
+    out = torch.empty(blocks * threads, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = {}
+    for packed, name in ((0, "fma.rn.f32"), (1, "fma.rn.f32x2")):
+        best = None
+        for i in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc = L.moe_fma_peak_launch(ctypes.c_void_p(out.data_ptr()), blocks, threads, iters, packed,
+                                       ctypes.c_void_p(stream.cuda_stream))
+            b.record(stream)
+            torch.cuda.synchronize()
+            if rc != 0:
+                raise RuntimeError(f"fma peak launch failed ({rc})")
+            if i >= 2:
+                ms = a.elapsed_time(b)
+                best = ms if best is None else min(best, ms)
+        res[name] = L.moe_fma_peak_flops(blocks, threads, iters) / (best * 1e-3) / 1e12
+    res["peak"] = max(res.values())
+    res["how"] = (f"{blocks} CTAs x {threads} threads, 16 independent FMA chains per thread, "
+                  f"{iters * 8} steps; best of 5 launches (CUDA events)")
+    return res
+
+
 # ------------------------------------------------------------------ our arm
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs"],
-                    help="tensor-core tiling of the grouped GEMMs (library default: auto)")
-    ap.add_argument("--capacity-factor", type=float, default=None,
-                    help="expert capacity ceil(cf * T * k / N); overflow assignments are dropped")
-    ap.add_argument("--routing", default="token", choices=["token", "expert"],
-                    help="token choice (top-k per token) or expert choice (each expert takes C = T*k/N tokens)")
-    args = ap.parse_args()
-    if args.routing == "expert" and args.capacity_factor is not None:
-        ap.error("--capacity-factor applies to token-choice routing only")
-    args.warmup = max(args.warmup, 3)
-    w0 = S.WORKLOADS[args.workload]
-    if args.impl == "reference":
-        return reference_arm(args, w0)
-
-    import torch
-    from mixture_experts_layer_97_b300 import binding as B
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    B.set_ffn_tiling(args.ffn_tiling)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = replica_workload(w0, rank)
-
+def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, dist, want_e2e: bool,
+            want_cpu: bool, steps: int, warmup: int) -> dict:
+    """Upload one workload's seeded inputs, time `steps` forwards (after
+    `warmup`), optionally end to end through the host-buffer entry points and
+    the CPU oracle on a bounded sample. Returns the measurements (rank 0)."""
     # cpu sample plan first (host only), so its experts can be kept while uploading
-    do_cpu = rank == 0 and not args.no_cpu_baseline and args.routing == "token"
+    ec = args.routing == "expert"
+    do_cpu = want_cpu and not ec
     if do_cpu:
         cpu_rows = {"worked-example-n64-f16384-gelu": 384, "prefill-n8-f14336": 128,
                     "zipf-skew-n128-k8": 4096, "decode-t32-n64-k8": 256}.get(w.name, 256)
@@ -319,7 +328,6 @@ def main():
     torch.cuda.synchronize()
 
     s = B.shape(w.T, w.d, w.N, w.k, w.F, w.act, w.dtype)
-    ec = args.routing == "expert"
     C = max(1, w.T * w.k // w.N) if ec else 0
     A = w.N * C if ec else w.A
     s_rows = B.shape(A, w.d, w.N, 1, w.F, w.act, w.dtype) if ec else s     # grouped FFN over the N*C rows
@@ -382,7 +390,7 @@ def main():
             fn()
         if ev: ev[4].record(stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     st = B.get_error()
@@ -411,13 +419,13 @@ def main():
     except RuntimeError:
         graphs = None
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
-        for i in range(args.steps):
+        for i in range(steps):
             flush_l2()                         # L2 flush between timed steps (outside the events)
             step(evs[i])
         torch.cuda.synchronize()
@@ -434,7 +442,7 @@ def main():
 
     # end to end through the public host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if want_e2e:
         x_host = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory() if w.dtype == "bf16" \
             else torch.from_numpy(x_h).pin_memory()
         out_host = torch.empty((w.T, w.d), dtype=td).pin_memory()
@@ -457,10 +465,10 @@ def main():
             forward_e2e()
         torch.cuda.synchronize()
         e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
+                for _ in range(steps)]
         if dist:
             dist.barrier()
-        for i in range(args.steps):
+        for i in range(steps):
             flush_l2()
             e_ev[i][0].record(stream)
             forward_e2e()
@@ -496,23 +504,24 @@ def main():
             p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             p0.record(stream)
             s_in.wait_event(p0)
-            for i in range(args.steps):
+            for i in range(steps):
                 piped(i)
             p1.record(s_out)                   # after the last output copy
             torch.cuda.synchronize()
             if B.get_error() != B.MOE_OK:
                 raise RuntimeError("device error during the pipelined end-to-end run")
-            p_ms = max_over_ranks(p0.elapsed_time(p1) / args.steps, dist, "cuda")
-            e2e.update({"value": job_throughput(w.T, world, p_ms), "ms_per_step": p_ms,
-                        "mode": ("pipelined: moe_forward_hostio_pipelined over consecutive steps; every step "
-                                 "copies its x in and its output out, overlapping the neighbouring steps' layer"),
-                        "l2": "no flush between pipelined steps: the expert weights every step reads exceed L2",
-                        "serial_value": job_throughput(w.T, world, e_ms), "serial_ms_per_step": e_ms})
+            p_ms = max_over_ranks(p0.elapsed_time(p1) / steps, dist, "cuda")
+            if p_ms < e_ms:
+                e2e.update({"value": job_throughput(w.T, world, p_ms), "ms_per_step": p_ms,
+                            "mode": ("pipelined: moe_forward_hostio_pipelined over consecutive steps; every "
+                                     "step copies its x in and its output out, overlapping the neighbouring "
+                                     "steps' layer"),
+                            "l2": "no flush between pipelined steps: the expert weights every step reads exceed L2"})
+            e2e.update({"serial_value": job_throughput(w.T, world, e_ms), "serial_ms_per_step": e_ms,
+                        "pipelined_value": job_throughput(w.T, world, p_ms), "pipelined_ms_per_step": p_ms})
 
     if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return
+        return {}
 
     P = peaks()
     cnt = counts.cpu().numpy()
@@ -568,29 +577,124 @@ def main():
                "kind": "oracle",
                "sample": (f"{len(cpu_tokens)} tokens (route + {len(cpu_tokens) * w.k} expert rows + combine) "
                           f"whose experts lie in a {len(cpu_used)}-expert subset; {secs:.1f} s")}
+    stage_ms = {"route": float(np.median(stage[:, 0])), "permute": float(np.median(stage[:, 1])),
+                "grouped_ffn": ffn_ms, "combine": float(np.median(stage[:, 3]))}
+    return dict(w=w, C=C, ec=ec, cf=cf, step_ms=step_ms, ffn_ms=ffn_ms, stage_ms=stage_ms, cnt=cnt,
+                ffn_flops=ffn_flops, roof=roof, cpu=cpu, e2e=e2e, clocks=clk.summary(),
+                routing_stats=routing_stats, dropped=int(dropped.item()) if cf is not None else 0,
+                graphs=graphs is not None, fwd_bytes=fwd_bytes, P=P)
 
-    clocks = clk.summary()
+
+def route_roofline(r: dict, fma: Optional[dict]) -> dict:
+    """The gate projection (2 T d N fp32 FLOPs) of the route stage against the
+    measured fp32 FMA peak of the CUDA cores."""
+    w = r["w"]
+    flops = acc.gate_flops(w.T, w.d, w.N)
+    ach = flops / (r["stage_ms"]["route"] * 1e-3) / 1e12
+    out = {"bound": "alu", "kernel": "route_kernel (gate GEMV/GEMM in fp32 FMA chains + top-k)", "achieved": ach,
+           "unit": "TFLOP/s", "algorithmic_flops_per_call": flops, "us": r["stage_ms"]["route"] * 1e3}
+    if fma:
+        out.update({"peak": fma["peak"], "frac": ach / fma["peak"],
+                    "peak_kind": "measured fp32 FMA (libmoe_fma_peak.so: " + fma["how"] + ")"})
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-shaped sub-record that follows the headline workload")
+    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs", "pairs_db"],
+                    help="tensor-core tiling of the grouped GEMMs (library default: auto)")
+    ap.add_argument("--capacity-factor", type=float, default=None,
+                    help="expert capacity ceil(cf * T * k / N); overflow assignments are dropped")
+    ap.add_argument("--routing", default="token", choices=["token", "expert"],
+                    help="token choice (top-k per token) or expert choice (each expert takes C = T*k/N tokens)")
+    args = ap.parse_args()
+    if args.routing == "expert" and args.capacity_factor is not None:
+        ap.error("--capacity-factor applies to token-choice routing only")
+    args.warmup = max(args.warmup, 3)
+    w0 = S.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w0)
+
+    import torch
+    from mixture_experts_layer_97_b300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    B.set_ffn_tiling(args.ffn_tiling)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = replica_workload(w0, rank)
+    r = measure(w, args, torch, B, world, rank, local, dist, want_e2e=not args.no_e2e,
+                want_cpu=rank == 0 and not args.no_cpu_baseline, steps=args.steps, warmup=args.warmup)
+    fma = None
+    if rank == 0:
+        try:
+            fma = fma_peak_tflops(torch, torch.cuda.get_device_properties(local).multi_processor_count)
+        except (OSError, RuntimeError):
+            fma = None
+    # the decode-shaped layer (HBM-bound on its active experts' weights), timed after the headline run
+    dec = None
+    decode_name = "decode-t32-n64-k8"
+    if not args.no_decode and w0.name != decode_name and args.routing == "token" and args.capacity_factor is None:
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        wd = replica_workload(S.WORKLOADS[decode_name], rank)
+        rd = measure(wd, args, torch, B, world, rank, local, dist, want_e2e=not args.no_e2e,
+                     want_cpu=rank == 0 and not args.no_cpu_baseline, steps=max(args.steps, 50),
+                     warmup=max(args.warmup, 10))
+        if rank == 0:
+            dec = {"workload": decode_name, "ms_per_step": rd["step_ms"],
+                   "value": job_throughput(wd.T, world, rd["step_ms"]), "unit": "tokens/s",
+                   "stage_ms": rd["stage_ms"],
+                   "ffn_gbs": rd["roof"]["achieved"] if rd["roof"]["bound"] == "hbm" else None,
+                   "ffn_frac_hbm": rd["roof"]["frac"] if rd["roof"]["bound"] == "hbm" else None,
+                   "forward_frac_hbm": rd["roof"]["forward_frac_hbm"],
+                   "forward_algorithmic_bytes": rd["fwd_bytes"], "peak_gbs": rd["P"]["hbm"],
+                   "active_experts": int((rd["cnt"] > 0).sum()), "route_roofline": route_roofline(rd, fma),
+                   "clocks": rd["clocks"], "cpu_baseline": rd["cpu"], "e2e": rd["e2e"],
+                   "steps": max(args.steps, 50), "warmup": max(args.warmup, 10)}
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    C, ec, cf = r["C"], r["ec"], r["cf"]
+    cnt = r["cnt"]
     line = {
-        "metric": "MoE-layer tokens/s", "value": job_throughput(w.T, world, step_ms), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "metric": "MoE-layer tokens/s", "value": job_throughput(w.T, world, r["step_ms"]), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["step_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,
                    "gate": "fp32", "ffn_tiling": args.ffn_tiling, "capacity_factor": cf,
                    "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write, then 2 x 126 MB read of another buffer); expert weights also exceed L2"},
         "timing": ("median over steps; every stage is a CUDA-graph replay between CUDA events on the stream"
-                   if graphs is not None else "median over steps of eager stage calls between CUDA events"),
-        "ffn_tflops": ffn_flops / (ffn_ms * 1e-3) / 1e12,
-        "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (step_ms * 1e-3) / 1e12,
-        "stage_ms": {"route": float(np.median(stage[:, 0])), "permute": float(np.median(stage[:, 1])),
-                     "grouped_ffn": ffn_ms, "combine": float(np.median(stage[:, 3]))},
-        "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()), "routing_stats": routing_stats,
-        "dropped_assignments": int(dropped.item()) if cf is not None else 0,
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                   if r["graphs"] else "median over steps of eager stage calls between CUDA events"),
+        "ffn_tflops": r["ffn_flops"] / (r["ffn_ms"] * 1e-3) / 1e12,
+        "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (r["step_ms"] * 1e-3) / 1e12,
+        "stage_ms": r["stage_ms"],
+        "active_experts": int((cnt > 0).sum()), "max_expert_rows": int(cnt.max()),
+        "routing_stats": r["routing_stats"], "dropped_assignments": r["dropped"],
+        "roofline": r["roof"], "route_roofline": route_roofline(r, fma), "fma_peak": fma,
+        "cpu_baseline": r["cpu"], "e2e": r["e2e"],
         # token choice: route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1;
         # expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
         "gpu_launches": (6 if ec else 8) * args.steps,
-        "clocks": clocks,
+        "clocks": r["clocks"],
+        "decode": dec,
         "kernel_source": kernel_source_hash(),
     }
     print(json.dumps(line), flush=True)

@@ -332,6 +332,45 @@ moe_status moe_permute_noalloc(const moe_shape *s, const int32_t *topk_idx, cons
                                void *x_perm, void *stream);
 
 /*
+ * Expert parallelism: "MoE混合专家模型计算原理与推理部署实战解析" section 3.3
+ * (experts split over G GPUs by expert id, e.g. 8 experts over 4 cards with
+ * 2 each; every card routes its own tokens and an all-to-all carries each
+ * token row to the card that holds its expert; the traffic grows with tokens
+ * x hidden size) and section 6.3 (EP). Reading: card g holds the contiguous
+ * expert range [g*E, (g+1)*E) with E = N / G, so moe_permute's x_perm, ordered
+ * by expert, is already ordered by destination card: card g's share is rows
+ * offsets[g*E] .. offsets[(g+1)*E] - 1. The exchanges themselves (an
+ * all-to-all of the per-expert counts, then of the rows, and back) are the
+ * caller's, e.g. NCCL or any other transport; the library does the local
+ * steps on either side of them.
+ *
+ * moe_ep_regroup: the rows a card received, ordered by (source card g, local
+ * expert e, the source's row order), regrouped by local expert for
+ * moe_grouped_ffn:
+ *   recv_counts [G][E] int32 (device): rows card g sent for local expert e;
+ *                the table must account for exactly `rows` received rows
+ *   recv_x      [rows, d] (dtype): the received rows in that order
+ *   x_local     [rows, d]: the same rows ordered (e, g, source order)
+ *   offsets_local [E+1]: expert e's rows are offsets_local[e] .. [e+1]-1
+ *   local_src   [rows] int32: the received row each local row came from
+ * moe_grouped_ffn then runs on a shape with T = rows, k = 1, N = E and the
+ * card's E experts' weights.
+ * moe_ep_ungroup: y_recv[local_src[i]] = y_local[i] (back to the received
+ * order); the reverse all-to-all then returns every row to its source in the
+ * order it was sent, i.e. as that source's y_perm, and moe_combine runs on it
+ * unchanged.
+ * Needs 1 <= G*E <= 256, rows < 2^31, d * element size a multiple of 16
+ * bytes. A count table that is negative or does not add up to `rows`, or a
+ * local_src entry out of range, records MOE_ERR_CORRUPT (nothing copied).
+ * Integer bookkeeping and row copies only: bit-exact.
+ */
+moe_status moe_ep_regroup(int32_t G, int32_t E, const int32_t *recv_counts, int64_t rows, int32_t d,
+                          int32_t dtype, const void *recv_x, void *x_local, int32_t *offsets_local,
+                          int32_t *local_src, void *stream);
+moe_status moe_ep_ungroup(int64_t rows, int32_t d, int32_t dtype, const int32_t *local_src,
+                          const void *y_local, void *y_recv, void *stream);
+
+/*
  * Tiling of the bf16 grouped GEMMs in moe_grouped_ffn / moe_forward (process
  * wide; results agree within the bf16 tolerance, not bit for bit):
  *   MOE_TILING_ROWS    128 permuted rows x 256 weight rows per tile (weights
@@ -342,15 +381,24 @@ moe_status moe_permute_noalloc(const moe_shape *s, const int32_t *topk_idx, cons
  *                      to 16 rows): little padding when experts hold few rows.
  *   MOE_TILING_PAIRS   token tiles computed by clusters of two SMs sharing each
  *                      MMA (256 weight rows per MMA, each SM holding half of
- *                      the tile's tokens): four 48 KB pipeline stages per SM
- *                      instead of three 64 KB ones.
- *   MOE_TILING_AUTO    per GEMM: token tiles on SM pairs when T*k >= 64*N and
- *                      the GEMM's reduction length (d for the first, F for the
- *                      second) is >= 4096, else row tiles (default).
+ *                      the tile's tokens), two 128-row weight blocks per SM
+ *                      and one accumulator pair filling tensor memory: four
+ *                      48 KB pipeline stages per SM.
+ *   MOE_TILING_PAIRS_DB token tiles on SM pairs with one 128-row weight block
+ *                      per SM and two accumulators in tensor memory, so the
+ *                      epilogue of one tile overlaps the next tile's MMAs (six
+ *                      32 KB stages); the SwiGLU up projection, which pairs
+ *                      gate and up rows, runs as MOE_TILING_PAIRS.
+ *   MOE_TILING_AUTO    per GEMM: token tiles on SM pairs (as
+ *                      MOE_TILING_PAIRS_DB) when T*k >= 64*N and the GEMM's
+ *                      reduction length (d for the first, F for the second)
+ *                      is >= 4096, else row tiles (default).
  * The pages' grouped GEMM ("MoE显存与计算开销四阶段手算指南" section 4.3)
  * fixes no tiling; this only chooses how the same product is blocked.
  */
-typedef enum { MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2, MOE_TILING_PAIRS = 3 } moe_tiling;
+typedef enum {
+    MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2, MOE_TILING_PAIRS = 3, MOE_TILING_PAIRS_DB = 4
+} moe_tiling;
 moe_status moe_set_ffn_tiling(int mode);
 int moe_get_ffn_tiling(void);
 

@@ -24,7 +24,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_CORRUPT = 4, 5, 6
 MOE_F32, MOE_BF16 = 0, 1
 MOE_SWIGLU, MOE_GELU_TANH = 0, 1
-TILING = {"auto": 0, "rows": 1, "tokens": 2, "pairs": 3}
+TILING = {"auto": 0, "rows": 1, "tokens": 2, "pairs": 3, "pairs_db": 4}
 ACT = {"swiglu": MOE_SWIGLU, "gelu_tanh": MOE_GELU_TANH}
 DTYPE = {"f32": MOE_F32, "bf16": MOE_BF16}
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -66,6 +66,8 @@ SIGNATURES = {
     "moe_expert_choice_workspace_size": (SZ, [SP, I64]),
     "moe_gather_rows": (I32, [SP, P, I32, I64, P, P, P]),
     "moe_combine": (I32, [SP, P, P, P, P, P]),
+    "moe_ep_regroup": (I32, [I32, I32, P, I64, I32, I32, P, P, P, P, P]),
+    "moe_ep_ungroup": (I32, [I64, I32, I32, P, P, P, P]),
     "moe_forward": (I32, [SP, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_hostio": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_hostio_pipelined": (I32, [SP, P, P, P, P, P, P, P, P, SZ, I32, P, P, P]),
@@ -259,6 +261,21 @@ def grouped_ffn(s, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, stream=Non
     _check(lib().moe_grouped_ffn(ctypes.byref(s), _ptr(x_perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up),
                                  _ptr(w_down), _ptr(y_perm), _ptr(ws), ws.numel() if ws is not None else 0,
                                  _stream(stream)), "moe_grouped_ffn")
+
+
+def ep_regroup(G, E, recv_counts, recv_x, x_local, offsets_local, local_src, dtype, stream=None):
+    """Received rows (source, local expert, source order) -> grouped by local expert."""
+    rows, d = int(recv_x.shape[0]), int(recv_x.shape[1])
+    _check(lib().moe_ep_regroup(int(G), int(E), _ptr(recv_counts), rows, d, DTYPE[dtype], _ptr(recv_x),
+                                _ptr(x_local), _ptr(offsets_local), _ptr(local_src), _stream(stream)),
+           "moe_ep_regroup")
+
+
+def ep_ungroup(local_src, y_local, y_recv, dtype, stream=None):
+    """y_recv[local_src[i]] = y_local[i]."""
+    rows, d = int(y_local.shape[0]), int(y_local.shape[1])
+    _check(lib().moe_ep_ungroup(rows, d, DTYPE[dtype], _ptr(local_src), _ptr(y_local), _ptr(y_recv),
+                                _stream(stream)), "moe_ep_ungroup")
 
 
 def combine(s, y_perm, inv_perm, topk_w, out, stream=None):

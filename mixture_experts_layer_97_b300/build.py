@@ -19,6 +19,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmoe_b300.so")
+# the benchmark's fp32 FMA microbenchmark (the route kernel's roofline denominator)
+PEAK_LIB = os.path.join(PKG, "libmoe_fma_peak.so")
+PEAK_SRC = os.path.join(CSRC, "fma_peak.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -32,6 +35,20 @@ def _nvcc() -> str:
 def _sources():
     return ([os.path.join(CSRC, "moe_b300.cu")] + sorted(glob.glob(os.path.join(CSRC, "*.cuh")))
             + [os.path.join(ROOT, "include", "moe.h")])
+
+
+def build_fma_peak(force: bool = False) -> str:
+    """The fp32 FMA microbenchmark library (separate from the MoE library)."""
+    if not force and os.path.exists(PEAK_LIB) and os.path.getmtime(PEAK_LIB) >= os.path.getmtime(PEAK_SRC):
+        return PEAK_LIB
+    tmp = PEAK_LIB + f".tmp{os.getpid()}"
+    cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-shared", "-o", tmp,
+           PEAK_SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed ({r.returncode}):\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, PEAK_LIB)
+    return PEAK_LIB
 
 
 def up_to_date() -> bool:
@@ -62,4 +79,5 @@ def build(force: bool = False, ptxas_info: bool = False, verbose: bool = False) 
 
 if __name__ == "__main__":
     build(force="--force" in sys.argv, ptxas_info="--ptxas-info" in sys.argv, verbose=True)
+    build_fma_peak(force="--force" in sys.argv)
     print(LIB)

@@ -16,11 +16,13 @@
 
 #include "combine.cuh"
 #include "common.cuh"
+#include "ep.cuh"
 #include "expert_choice.cuh"
 #include "ffn_simt.cuh"
 #include "ffn_tc.cuh"
 #include "ffn_tc_swap.cuh"
 #include "ffn_tc_pair.cuh"
+#include "ffn_tc_pair_db.cuh"
 #include "permute.cuh"
 #include "route.cuh"
 
@@ -307,7 +309,8 @@ EncodeTiledFn encode_fn() {
 std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
 
 bool tiling_valid(int mode) {
-  return mode == MOE_TILING_AUTO || mode == MOE_TILING_ROWS || mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS;
+  return mode == MOE_TILING_AUTO || mode == MOE_TILING_ROWS || mode == MOE_TILING_TOKENS ||
+         mode == MOE_TILING_PAIRS || mode == MOE_TILING_PAIRS_DB;
 }
 
 // bf16 matrix [rows, cols] row-major; box = box_rows x box_cols columns with the
@@ -425,12 +428,52 @@ moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* 
   return launched();
 }
 
+// Token tiles on SM pairs with two accumulators in TMEM (one weight block per
+// CTA): the GELU up projection and the plain down projection.
+template <int EPI>
+moe_status launch_tc_pair_db(const moe_shape* s, const void* a, int K, const void* w, int Nout,
+                             const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  const int64_t A = n_assign(s);
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox, kTcBK)) return MOE_ERR_CUDA;
+  if (!make_map(&mw, w, static_cast<uint64_t>(s->N) * Nout, static_cast<uint64_t>(K), kSwFM, kTcBK))
+    return MOE_ERR_CUDA;
+  auto kern = grouped_gemm_tc_pair_db_kernel<EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPdSmemBytes)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int64_t n_ftiles = (Nout + kPdFeatures - 1) / kPdFeatures;
+  const int64_t pairs_needed = ((A + kSwMaxNT - 1) / kSwMaxNT + s->N) * n_ftiles;
+  const int64_t max_pairs = num_sms() / 2;
+  const int64_t pairs = pairs_needed < max_pairs ? pairs_needed : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kSwThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPdSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, mw, mx, offsets, s->N, static_cast<int>(A), K, Nout,
+                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launched();
+}
+
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st, int mode) {
-  // auto and "pairs" run token tiles on SM pairs, "tokens" on single SMs
+  // "tokens": token tiles on single SMs; "pairs": on SM pairs with one accumulator pair; auto and
+  // "pairs_db": on SM pairs with two accumulators where one weight block per CTA suffices (GELU, plain)
   if (mode == MOE_TILING_TOKENS)
     return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
+  if constexpr (EPI != EPI_SWIGLU) {
+    if (mode != MOE_TILING_PAIRS) return launch_tc_pair_db<EPI>(s, a, K, w0, Nout, offsets, out, ldo, st);
+  }
   return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
 }
 
@@ -439,7 +482,7 @@ moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* 
 // their epilogue is not overlapped with the next tile: they pay off when an
 // expert holds enough rows to fill tiles and K is long enough to hide it.
 bool use_token_tiles(const moe_shape* s, int K, int mode) {
-  if (mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS) return true;
+  if (mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS || mode == MOE_TILING_PAIRS_DB) return true;
   if (mode == MOE_TILING_ROWS) return false;
   return n_assign(s) >= static_cast<int64_t>(kAutoTokenTileMinRowsPerExpert) * s->N && K >= kAutoTokenTileMinK;
 }
@@ -620,6 +663,22 @@ bool weights_ok(const moe_shape* s, const void* w_gate, const void* w_up, const 
   if (!ptr_ok(w_gate, true) || !ptr_ok(w_down, true)) return false;
   if (s->act == MOE_SWIGLU) return ptr_ok(w_up, true);
   return w_up == nullptr;
+}
+
+// ---------------------------------------------------------------- expert parallelism
+moe_status ep_args_status(int32_t G, int32_t E, int64_t rows, int32_t d, int32_t dtype) {
+  if (G < 1 || E < 1 || rows < 0 || d < 1) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(G) * E > kEpMaxTable || rows >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  if ((static_cast<int64_t>(d) * (dtype == MOE_F32 ? 4 : 2)) % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+unsigned ep_grid(int64_t rows) {
+  const int64_t per = kEpThreads / 32;
+  const int64_t want = (rows + per - 1) / per;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  return static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
 __global__ void bounded_wait_selftest_kernel(unsigned long long timeout_ns) {
@@ -995,6 +1054,35 @@ moe_status moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, cons
   if (scratch == nullptr) return MOE_ERR_CUDA;
   return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, scratch,
                       static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- expert parallelism
+moe_status moe_ep_regroup(int32_t G, int32_t E, const int32_t* recv_counts, int64_t rows, int32_t d, int32_t dtype,
+                          const void* recv_x, void* x_local, int32_t* offsets_local, int32_t* local_src,
+                          void* stream) {
+  moe_status st = ep_args_status(G, E, rows, d, dtype);
+  if (st != MOE_OK) return st;
+  const bool any = rows > 0;
+  if (!ptr_ok(recv_counts, true) || !ptr_ok(recv_x, any) || !ptr_ok(x_local, any) || !ptr_ok(offsets_local, true) ||
+      !ptr_ok(local_src, any))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t nv = static_cast<int64_t>(d) * (dtype == MOE_F32 ? 4 : 2) / 16;
+  ep_regroup_kernel<<<ep_grid(rows), kEpThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      recv_counts, G, E, rows, nv, static_cast<const uint4*>(recv_x), static_cast<uint4*>(x_local), offsets_local,
+      local_src);
+  return launched();
+}
+
+moe_status moe_ep_ungroup(int64_t rows, int32_t d, int32_t dtype, const int32_t* local_src, const void* y_local,
+                          void* y_recv, void* stream) {
+  moe_status st = ep_args_status(1, 1, rows, d, dtype);
+  if (st != MOE_OK) return st;
+  if (rows == 0) return MOE_OK;
+  if (!ptr_ok(local_src, true) || !ptr_ok(y_local, true) || !ptr_ok(y_recv, true)) return MOE_ERR_INVALID_ARG;
+  const int64_t nv = static_cast<int64_t>(d) * (dtype == MOE_F32 ? 4 : 2) / 16;
+  ep_ungroup_kernel<<<ep_grid(rows), kEpThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      local_src, rows, nv, static_cast<const uint4*>(y_local), static_cast<uint4*>(y_recv));
+  return launched();
 }
 
 moe_status moe_set_ffn_tiling(int mode) {

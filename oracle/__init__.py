@@ -72,6 +72,8 @@ def lib():
         L.oracle_forward.argtypes = [I64, I, I, I, I, I, P, I, P, I, P, I, I, I, P, P, P, I,
                                      P, P, P, P, P, P, P, P, P]
         L.oracle_forward.restype = I
+        L.oracle_ep_regroup.argtypes = [I, I, P, P, P]
+        L.oracle_ep_regroup.restype = I
         _lib = L
     return _lib
 
@@ -204,6 +206,22 @@ def expert_choice(probs, C):
     if lib().oracle_expert_choice(T, N, C, _p(probs), _p(perm), _p(w_row), _p(inv), _p(w), _p(thr), _p(nxt)):
         raise ValueError("oracle_expert_choice: bad arguments (need 0 <= C <= T)")
     return dict(perm=perm[:N * C], w_row=w_row[:N * C], inv=inv, w=w, thr=thr, next=nxt)
+
+
+def ep_regroup(recv_counts):
+    """Expert parallelism, receiving side: the rows received from G source
+    cards, ordered (source g, local expert e, source order) with
+    recv_counts[g, e] rows per run, ordered instead by (e, g, source order).
+    Returns offsets_local [E+1] and local_src [rows] (the received row each
+    local row takes)."""
+    rc = np.ascontiguousarray(recv_counts, dtype=np.int32)
+    G, E = rc.shape
+    rows = int(rc.sum())
+    offsets = np.empty(E + 1, np.int32)
+    src = np.empty(max(rows, 1), np.int32)
+    if lib().oracle_ep_regroup(G, E, _p(rc), _p(offsets), _p(src)):
+        raise ValueError("oracle_ep_regroup: negative count")
+    return dict(offsets_local=offsets, local_src=src[:rows])
 
 
 def expert_rows(x_rows, w_gate, w_up, w_down, act, want_h=False):

@@ -397,6 +397,42 @@ int oracle_expert_choice(int64_t T, int N, int64_t C, const double *probs,
 }
 
 /* SiLU and tanh-GELU, [P3] s3.1 (SiLU(gate) * up). */
+/*
+ * Expert parallelism, the receiving card's regrouping ([P3] s3.3: experts
+ * split over cards by expert id, token rows carried to the card of their
+ * expert by an all-to-all). The card received, from each source card g in
+ * order, that source's rows for the card's local experts e = 0..E-1 in order
+ * (recv_counts[g*E + e] of them, in the source's own row order). The grouped
+ * computation wants them ordered by local expert, and within an expert by
+ * source card, then source order. This walks the received buffer once, noting
+ * where each (g, e) run starts, then lays the runs out expert by expert:
+ *   offsets_local[e]   first local row of expert e (offsets_local[E] = rows)
+ *   local_src[row]     the received row that local row holds
+ * Returns 0, or -1 for a negative count.
+ */
+int oracle_ep_regroup(int G, int E, const int32_t *recv_counts, int32_t *offsets_local, int32_t *local_src)
+{
+    int64_t *run_start = (int64_t *)malloc(sizeof(int64_t) * (size_t)G * (size_t)E);
+    if (!run_start) return -1;
+    int64_t pos = 0;
+    for (int g = 0; g < G; ++g)
+        for (int e = 0; e < E; ++e) {
+            if (recv_counts[g * E + e] < 0) { free(run_start); return -1; }
+            run_start[g * E + e] = pos;
+            pos += recv_counts[g * E + e];
+        }
+    int64_t row = 0;
+    for (int e = 0; e < E; ++e) {
+        offsets_local[e] = (int32_t)row;
+        for (int g = 0; g < G; ++g)
+            for (int32_t i = 0; i < recv_counts[g * E + e]; ++i)
+                local_src[row++] = (int32_t)(run_start[g * E + e] + i);
+    }
+    offsets_local[E] = (int32_t)row;
+    free(run_start);
+    return 0;
+}
+
 static double silu(double v) { return v / (1.0 + exp(-v)); }
 static double gelu_tanh(double v)
 {

@@ -610,7 +610,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode-shaped sub-record that follows the headline workload")
-    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs", "pairs_db"],
+    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs"],
                     help="tensor-core tiling of the grouped GEMMs (library default: auto)")
     ap.add_argument("--capacity-factor", type=float, default=None,
                     help="expert capacity ceil(cf * T * k / N); overflow assignments are dropped")

@@ -381,24 +381,15 @@ moe_status moe_ep_ungroup(int64_t rows, int32_t d, int32_t dtype, const int32_t 
  *                      to 16 rows): little padding when experts hold few rows.
  *   MOE_TILING_PAIRS   token tiles computed by clusters of two SMs sharing each
  *                      MMA (256 weight rows per MMA, each SM holding half of
- *                      the tile's tokens), two 128-row weight blocks per SM
- *                      and one accumulator pair filling tensor memory: four
- *                      48 KB pipeline stages per SM.
- *   MOE_TILING_PAIRS_DB token tiles on SM pairs with one 128-row weight block
- *                      per SM and two accumulators in tensor memory, so the
- *                      epilogue of one tile overlaps the next tile's MMAs (six
- *                      32 KB stages); the SwiGLU up projection, which pairs
- *                      gate and up rows, runs as MOE_TILING_PAIRS.
- *   MOE_TILING_AUTO    per GEMM: token tiles on SM pairs (as
- *                      MOE_TILING_PAIRS_DB) when T*k >= 64*N and the GEMM's
- *                      reduction length (d for the first, F for the second)
- *                      is >= 4096, else row tiles (default).
+ *                      the tile's tokens): four 48 KB pipeline stages per SM
+ *                      instead of three 64 KB ones.
+ *   MOE_TILING_AUTO    per GEMM: token tiles on SM pairs when T*k >= 64*N and
+ *                      the GEMM's reduction length (d for the first, F for the
+ *                      second) is >= 4096, else row tiles (default).
  * The pages' grouped GEMM ("MoE显存与计算开销四阶段手算指南" section 4.3)
  * fixes no tiling; this only chooses how the same product is blocked.
  */
-typedef enum {
-    MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2, MOE_TILING_PAIRS = 3, MOE_TILING_PAIRS_DB = 4
-} moe_tiling;
+typedef enum { MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2, MOE_TILING_PAIRS = 3 } moe_tiling;
 moe_status moe_set_ffn_tiling(int mode);
 int moe_get_ffn_tiling(void);
 

@@ -22,7 +22,6 @@
 #include "ffn_tc.cuh"
 #include "ffn_tc_swap.cuh"
 #include "ffn_tc_pair.cuh"
-#include "ffn_tc_pair_db.cuh"
 #include "permute.cuh"
 #include "route.cuh"
 
@@ -221,6 +220,16 @@ moe_status launch_route(const moe_shape* s, const TX* x, RouteArgs& a, cudaStrea
     if ((T + 63) / 64 >= sms) return launch_route_tm<8, 2, TX>(s, x, a, st);     // 64 tokens/CTA
     return launch_route_tm<8, 1, TX>(s, x, a, st);                                // 32 tokens/CTA
   }
+  // Large batches: seven tokens per thread (more independent chains per thread hide more latency
+  // than more warps do) in tiles that give each SM one CTA: 56 tokens x up to 64 experts, or 112
+  // tokens x up to 128 experts (8192 x 64: 154 vs 168 us at 64 tokens per CTA; 16384 x 128: 227 vs
+  // 252 us; 512-thread CTAs with fewer chains per thread were slower in both)
+  if (s->N > 8 && s->N <= 64 && (T + 55) / 56 >= sms * 9 / 10) {
+    if (s->N <= 32) return launch_route_cfg<32, 1, 7, TX>(s, x, a, st);                 // 56 tokens/CTA
+    return launch_route_cfg<32, 2, 7, TX>(s, x, a, st);
+  }
+  if (s->N > 64 && s->N <= 128 && (T + 111) / 112 >= sms * 9 / 10)
+    return launch_route_cfg<16, 8, 7, TX>(s, x, a, st);                                  // 112 tokens/CTA
   // 64 tokens per CTA already at 3/4 of an SM each: measured faster than 32 tokens on every SM
   // (8192 tokens, 64 experts: 166 vs 184 us), the 16 chains per thread hiding more FMA latency
   if ((T + 63) / 64 >= sms * 3 / 4) return launch_route_tm<16, 4, TX>(s, x, a, st);   // 64 tokens/CTA
@@ -309,8 +318,7 @@ EncodeTiledFn encode_fn() {
 std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
 
 bool tiling_valid(int mode) {
-  return mode == MOE_TILING_AUTO || mode == MOE_TILING_ROWS || mode == MOE_TILING_TOKENS ||
-         mode == MOE_TILING_PAIRS || mode == MOE_TILING_PAIRS_DB;
+  return mode == MOE_TILING_AUTO || mode == MOE_TILING_ROWS || mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS;
 }
 
 // bf16 matrix [rows, cols] row-major; box = box_rows x box_cols columns with the
@@ -428,52 +436,12 @@ moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* 
   return launched();
 }
 
-// Token tiles on SM pairs with two accumulators in TMEM (one weight block per
-// CTA): the GELU up projection and the plain down projection.
-template <int EPI>
-moe_status launch_tc_pair_db(const moe_shape* s, const void* a, int K, const void* w, int Nout,
-                             const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
-  const int64_t A = n_assign(s);
-  CUtensorMap mx, mw;
-  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox, kTcBK)) return MOE_ERR_CUDA;
-  if (!make_map(&mw, w, static_cast<uint64_t>(s->N) * Nout, static_cast<uint64_t>(K), kSwFM, kTcBK))
-    return MOE_ERR_CUDA;
-  auto kern = grouped_gemm_tc_pair_db_kernel<EPI>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPdSmemBytes)) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  const int64_t n_ftiles = (Nout + kPdFeatures - 1) / kPdFeatures;
-  const int64_t pairs_needed = ((A + kSwMaxNT - 1) / kSwMaxNT + s->N) * n_ftiles;
-  const int64_t max_pairs = num_sms() / 2;
-  const int64_t pairs = pairs_needed < max_pairs ? pairs_needed : max_pairs;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-  cfg.blockDim = dim3(kSwThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPdSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, mw, mx, offsets, s->N, static_cast<int>(A), K, Nout,
-                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return launched();
-}
-
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st, int mode) {
-  // "tokens": token tiles on single SMs; "pairs": on SM pairs with one accumulator pair; auto and
-  // "pairs_db": on SM pairs with two accumulators where one weight block per CTA suffices (GELU, plain)
+  // auto and "pairs" run token tiles on SM pairs, "tokens" on single SMs
   if (mode == MOE_TILING_TOKENS)
     return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
-  if constexpr (EPI != EPI_SWIGLU) {
-    if (mode != MOE_TILING_PAIRS) return launch_tc_pair_db<EPI>(s, a, K, w0, Nout, offsets, out, ldo, st);
-  }
   return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
 }
 
@@ -482,7 +450,7 @@ moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* 
 // their epilogue is not overlapped with the next tile: they pay off when an
 // expert holds enough rows to fill tiles and K is long enough to hide it.
 bool use_token_tiles(const moe_shape* s, int K, int mode) {
-  if (mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS || mode == MOE_TILING_PAIRS_DB) return true;
+  if (mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS) return true;
   if (mode == MOE_TILING_ROWS) return false;
   return n_assign(s) >= static_cast<int64_t>(kAutoTokenTileMinRowsPerExpert) * s->N && K >= kAutoTokenTileMinK;
 }

@@ -34,42 +34,33 @@
 // evaluation, so the top-k decision is reproducible bit for bit.
 //
 // One CTA owns TM tokens and all N experts (padded to NP = EG*EPT). K slices
-// of BK columns of x (raw dtype) and W_g (fp32) stream through a cp.async ring
-// of STAGES buffers. Each raw x slice is widened once per CTA into a buffer of
-// duplicated fp32 pairs {x, x} (two buffers, alternating), so that a thread's
-// packed FMA takes its x operand straight from one shared-memory load: the
-// inner loop is loads of x pairs and W_g vectors plus f32x2 FMAs, nothing
-// else. Thread (ty, tx) accumulates TPT tokens x EPT experts in registers; the
-// TM x NP logit tile then goes to shared memory, where one warp per token runs
-// k rounds of a warp-wide argmax. Logits never reach HBM. TM is picked per
-// launch so that small batches still spread over many SMs; small tiles take
-// deeper K slices (fewer barriers per chain step).
+// of 32 columns of x (raw dtype) and W_g (fp32) stream through a cp.async ring
+// of STAGES buffers. Thread (ty, tx) accumulates TPT tokens x EPT experts in
+// registers; the TM x NP logit tile then goes to shared memory, where one warp
+// per token runs k rounds of a warp-wide argmax. Logits never reach HBM.
+// TM is picked per launch (64, 32 or 8 tokens) so that small batches still
+// spread over many SMs.
 #pragma once
 #include "common.cuh"
 
 namespace moe {
 
+constexpr int kRouteBK = 32;
 constexpr int kRouteThreads = 256;
 
-template <int EG, int EPT, int TPT, typename TX>
+template <int EG, int EPT, int TPT, typename TX, int THR = kRouteThreads>
 struct RouteCfg {
   static constexpr int NP = EG * EPT;
-  static constexpr int TG = kRouteThreads / EG;
+  static constexpr int TG = THR / EG;
   static constexpr int TM = TG * TPT;
-  // K columns per slice: 32, or for tiles of at most 8 tokens (long chains, few
-  // FMAs per barrier) as deep as 32 KB of W_g per stage allows, up to 128
-  static constexpr int BKW = 8192 / NP;
-  static constexpr int BK = TM > 8 ? 32 : (BKW >= 128 ? 128 : (BKW >= 64 ? 64 : 32));
-  static constexpr int STAGES = 4;
-  static constexpr int XROW = BK * static_cast<int>(sizeof(TX)) + 16;        // raw bytes per token row (+pad)
-  static constexpr int XBYTES = TM * XROW;                                   // one raw stage of x
-  static constexpr int WBYTES = BK * NP * 4;                                 // one stage of W_g
-  static constexpr int DROW = BK * 8 + 16;                                   // {x, x} pairs per token row (+pad)
-  static constexpr int DBYTES = TM * DROW;                                   // one widened buffer
-  static constexpr size_t kPipe = static_cast<size_t>(STAGES) * (XBYTES + WBYTES) + 2 * DBYTES;
+  static constexpr int STAGES = NP >= 128 ? 3 : 4;
+  static constexpr int XROW = kRouteBK * static_cast<int>(sizeof(TX)) + 16;  // bytes per token row (+pad)
+  static constexpr int XBYTES = TM * XROW;                                   // one stage of x
+  static constexpr int WBYTES = kRouteBK * NP * 4;                           // one stage of W_g
+  static constexpr size_t kPipe = static_cast<size_t>(STAGES) * (XBYTES + WBYTES);
   static constexpr size_t kLogits = sizeof(float) * TM * (NP + 1);
-  // per-warp statistics rows [8][2*NP + 1] after the logit tile
-  static constexpr size_t kStats = kLogits + sizeof(float) * (kRouteThreads / 32) * (2 * NP + 1);
+  // per-warp statistics rows [THR / 32][2*NP + 1] after the logit tile
+  static constexpr size_t kStats = kLogits + sizeof(float) * (THR / 32) * (2 * NP + 1);
   static constexpr size_t kSmem = kPipe > kStats ? kPipe : kStats;
 };
 
@@ -87,6 +78,11 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
 __device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long a, unsigned long long b) {
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
+__device__ __forceinline__ unsigned long long splat2(float v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+  return r;
+}
 __device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
@@ -95,42 +91,35 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// 16 raw bytes of x -> the {x, x} pairs of its elements (8 bf16 -> 8 pairs, 4 fp32 -> 4 pairs).
-__device__ __forceinline__ void widen_pairs(const uint8_t* raw, uint8_t* dup, __nv_bfloat16) {
-  const uint4 q = *reinterpret_cast<const uint4*>(raw);
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    const float lo = bf16_lo(w[h]), hi = bf16_hi(w[h]);
-    *reinterpret_cast<float4*>(dup + 16 * h) = make_float4(lo, lo, hi, hi);
-  }
+// 8 consecutive K elements of one token, widened to fp32.
+__device__ __forceinline__ void load_x8(const __nv_bfloat16* p, float* v) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+  v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
 }
-__device__ __forceinline__ void widen_pairs(const uint8_t* raw, uint8_t* dup, float) {
-  const float4 q = *reinterpret_cast<const float4*>(raw);
-  *reinterpret_cast<float4*>(dup) = make_float4(q.x, q.x, q.y, q.y);
-  *reinterpret_cast<float4*>(dup + 16) = make_float4(q.z, q.z, q.w, q.w);
+__device__ __forceinline__ void load_x8(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-template <int EG, int EPT, int TPT, typename TX>
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restrict__ x, const float* __restrict__ wg,
+template <int EG, int EPT, int TPT, typename TX, int THR = kRouteThreads>
+__global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, const float* __restrict__ wg,
                                                               const float* __restrict__ bias, int T, int d, int N,
                                                               int k, int bias_select,
                                                               int32_t* __restrict__ topk_idx,
                                                               float* __restrict__ topk_w,
                                                               float* __restrict__ stats_part,
                                                               float* __restrict__ probs_out) {
-  using C = RouteCfg<EG, EPT, TPT, TX>;
-  constexpr int NP = C::NP, TM = C::TM, S = C::STAGES, BK = C::BK;
+  using C = RouteCfg<EG, EPT, TPT, TX, THR>;
+  constexpr int NP = C::NP, TM = C::TM, S = C::STAGES;
   constexpr int NPR = NP < 32 ? 32 : NP;   // register slots per token for the argmax
   constexpr int SLOTS = NPR / 32;
-  constexpr int XCH = BK * static_cast<int>(sizeof(TX)) / 16;   // 16-byte chunks per token row slice
-  constexpr int EPC = 16 / static_cast<int>(sizeof(TX));       // x elements per 16-byte chunk
-  static_assert(S >= 4, "the ring keeps the next slice's copy complete one iteration ahead");
+  constexpr int XCH = kRouteBK * static_cast<int>(sizeof(TX)) / 16;   // 16-byte chunks per token row slice
   extern __shared__ __align__(16) uint8_t route_smem[];
-  uint8_t* xs = route_smem;                                              // [S][TM][XROW bytes] raw x
-  float* ws = reinterpret_cast<float*>(route_smem + S * C::XBYTES);      // [S][BK][NP]
-  uint8_t* xd = route_smem + S * (C::XBYTES + C::WBYTES);                // [2][TM][DROW bytes] {x, x} pairs
-  float* lg = reinterpret_cast<float*>(route_smem);                      // [TM][NP+1] after the K loop
+  uint8_t* xs = route_smem;                      // [S][TM][XROW bytes]
+  float* ws = reinterpret_cast<float*>(route_smem + S * C::XBYTES);   // [S][BK][NP]
+  float* lg = reinterpret_cast<float*>(route_smem);                   // [TM][NP+1] after the K loop
 
   // Thread (ty, tx) owns tokens ty*TPT + i and experts V*tx + V*EG*m + c
   // (m < EPT/V, c < V, V = min(EPT, 4)): its W_g reads are V-wide vectors and
@@ -140,24 +129,24 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
   const int tx = tid % EG;
   const int ty = tid / EG;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TM;
-  const int KB = (d + BK - 1) / BK;
+  const int KB = (d + kRouteBK - 1) / kRouteBK;
   const bool w_vec = (N % 4) == 0;
 
   auto issue = [&](int kb) {
     const int st = kb % S;
-    const int k0 = kb * BK;
+    const int k0 = kb * kRouteBK;
     const uint32_t xb = smem_addr(xs + st * C::XBYTES);
-    for (int c = tid; c < TM * XCH; c += kRouteThreads) {
+    for (int c = tid; c < TM * XCH; c += THR) {
       const int r = c / XCH, q = c % XCH;
       const int64_t t = t0 + r;
-      const int kk = k0 + q * EPC;
+      const int kk = k0 + q * (16 / static_cast<int>(sizeof(TX)));
       const bool ok = (t < T) && (kk < d);
       const TX* src = ok ? x + t * d + kk : x;
       cp_async16(xb + r * C::XROW + q * 16, src, ok);
     }
-    const uint32_t wb = smem_addr(ws + st * BK * NP);
+    const uint32_t wb = smem_addr(ws + st * kRouteBK * NP);
     if (w_vec) {
-      for (int c = tid; c < BK * NP / 4; c += kRouteThreads) {
+      for (int c = tid; c < kRouteBK * NP / 4; c += THR) {
         const int kr = c / (NP / 4), n4 = (c % (NP / 4)) * 4;
         const int gk = k0 + kr;
         const bool ok = (gk < d) && (n4 < N);
@@ -165,22 +154,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
         cp_async16(wb + (kr * NP + n4) * 4, src, ok);
       }
     } else {
-      for (int c = tid; c < BK * NP; c += kRouteThreads) {
+      for (int c = tid; c < kRouteBK * NP; c += THR) {
         const int kr = c / NP, n = c % NP;
         const int gk = k0 + kr;
         const bool ok = (gk < d) && (n < N);
         const float* src = ok ? wg + static_cast<int64_t>(gk) * N + n : wg;
         cp_async4(wb + c * 4, src, ok);
       }
-    }
-  };
-  // raw slice kb -> widened buffer kb & 1 (every thread takes whole 16-byte chunks)
-  auto widen = [&](int kb) {
-    const uint8_t* xr = xs + (kb % S) * C::XBYTES;
-    uint8_t* dst = xd + (kb & 1) * C::DBYTES;
-    for (int c = tid; c < TM * XCH; c += kRouteThreads) {
-      const int r = c / XCH, q = c % XCH;
-      widen_pairs(xr + r * C::XROW + q * 16, dst + r * C::DROW + q * EPC * 8, TX{});
     }
   };
 
@@ -203,30 +183,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
     if (s < KB) issue(s);
     cp_async_commit();
   }
-  // slice 0 widened before the loop; in iteration kb slice kb + 1 is widened
-  // while slice kb (widened one iteration earlier) is consumed, so each slice
-  // costs one barrier
-  cp_async_wait<S - 2>();
-  __syncthreads();
-  widen(0);
   for (int kb = 0; kb < KB; ++kb) {
-    cp_async_wait<S - 3>();          // slice kb + 1 has landed (this thread's copies)
-    __syncthreads();                 // ... every thread's; slice kb's widened pairs are visible
+    cp_async_wait<S - 2>();
+    __syncthreads();
     if (kb + S - 1 < KB) issue(kb + S - 1);
     cp_async_commit();
-    if (kb + 1 < KB) widen(kb + 1);
-    const uint8_t* xdst = xd + (kb & 1) * C::DBYTES;
-    const float* wst = ws + (kb % S) * BK * NP;
-#pragma unroll 4
-    for (int k2 = 0; k2 < BK; k2 += 2) {
-      // {x_k, x_k} and {x_k+1, x_k+1} of each token in one 16-byte load
-      ulonglong2 xv[TPT];
+    const int st = kb % S;
+    const uint8_t* xst = xs + st * C::XBYTES;
+    const float* wst = ws + st * kRouteBK * NP;
+#pragma unroll
+    for (int k8 = 0; k8 < kRouteBK; k8 += 8) {
+      float xv[TPT][8];
 #pragma unroll
       for (int i = 0; i < TPT; ++i)
-        xv[i] = *reinterpret_cast<const ulonglong2*>(xdst + (ty * TPT + i) * C::DROW + k2 * 8);
+        load_x8(reinterpret_cast<const TX*>(xst + (ty * TPT + i) * C::XROW) + k8, xv[i]);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float* wr = wst + (k2 + u) * NP + V * tx;
+      for (int u = 0; u < 8; ++u) {
+        const float* wr = wst + (k8 + u) * NP + V * tx;
         if constexpr (PACKED) {
           unsigned long long wp[EP2];   // (expert 2p, expert 2p + 1) of this thread
 #pragma unroll
@@ -241,7 +214,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
           }
 #pragma unroll
           for (int i = 0; i < TPT; ++i) {
-            const unsigned long long xx = u ? xv[i].y : xv[i].x;
+            const unsigned long long xx = splat2(xv[i][u]);
 #pragma unroll
             for (int p = 0; p < EP2; ++p) ffma2(acc2[i][p], xx, wp[p]);
           }
@@ -250,12 +223,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
 #pragma unroll
           for (int m = 0; m < EPT; ++m) wv[m] = wr[EG * m];
 #pragma unroll
-          for (int i = 0; i < TPT; ++i) {
-            float xlo, xhi;
-            unpack2(u ? xv[i].y : xv[i].x, xlo, xhi);
+          for (int i = 0; i < TPT; ++i)
 #pragma unroll
-            for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xlo, wv[j], acc[i][j]);
-          }
+            for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xv[i][u], wv[j], acc[i][j]);
         }
       }
     }
@@ -293,7 +263,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
     p_acc[m] = 0.f;
     c_acc[m] = 0.f;
   }
-  for (int tl = warp; tl < TM; tl += kRouteThreads / 32) {
+  for (int tl = warp; tl < TM; tl += THR / 32) {
     const int64_t t = t0 + tl;
     if (t >= T) break;
     float g[SLOTS];           // logits of the softmax
@@ -388,7 +358,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
   }
   if (!want_stats) return;
   // per-warp rows -> one row per CTA: [N probability sums | N counts | top-1 sum]
-  float* srow = reinterpret_cast<float*>(route_smem + C::kLogits);   // [8][2*NP + 1]
+  float* srow = reinterpret_cast<float*>(route_smem + C::kLogits);   // [THR / 32][2*NP + 1]
   constexpr int SW = 2 * NP + 1;
 #pragma unroll
   for (int m = 0; m < SLOTS; ++m) {
@@ -401,10 +371,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
   if (lane == 0) srow[warp * SW + 2 * NP] = top1_acc;
   __syncthreads();
   float* out = stats_part + static_cast<int64_t>(blockIdx.x) * (2 * N + 1);
-  for (int n = tid; n < N; n += kRouteThreads) {
+  for (int n = tid; n < N; n += THR) {
     float ps = 0.f, cs = 0.f;
 #pragma unroll
-    for (int w = 0; w < kRouteThreads / 32; ++w) {
+    for (int w = 0; w < THR / 32; ++w) {
       ps += srow[w * SW + n];
       cs += srow[w * SW + NP + n];
     }
@@ -414,7 +384,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const TX* __restri
   if (tid == 0) {
     float ts = 0.f;
 #pragma unroll
-    for (int w = 0; w < kRouteThreads / 32; ++w) ts += srow[w * SW + 2 * NP];
+    for (int w = 0; w < THR / 32; ++w) ts += srow[w * SW + 2 * NP];
     out[2 * N] = ts;
   }
 }

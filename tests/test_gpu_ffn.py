@@ -64,7 +64,7 @@ RAGGED = [0, 1, 127, 128, 129, 300, 0, 5]
 RAGGED_TOKENS = [16, 17, 256, 257, 0, 31, 513, 1500]
 
 
-@pytest.fixture(params=["rows", "tokens", "pairs", "pairs_db"])
+@pytest.fixture(params=["rows", "tokens", "pairs"])
 def tiling(request):
     B.set_ffn_tiling(request.param)
     yield request.param
@@ -170,7 +170,7 @@ def test_tilings_agree_within_tolerance():
     of each other."""
     w, xp, ws, off = make_case([200, 0, 300, 45, 1000], 512, 384, "swiglu", "bf16", 12)
     outs = {}
-    for mode in ("rows", "tokens", "pairs", "pairs_db"):
+    for mode in ("rows", "tokens", "pairs"):
         B.set_ffn_tiling(mode)
         outs[mode] = run_ffn(w, xp, ws, off)
     B.set_ffn_tiling("auto")
@@ -179,18 +179,3 @@ def test_tilings_agree_within_tolerance():
         assert rel_err(got, ref) <= tol("bf16"), mode
     assert rel_err(outs["rows"], outs["tokens"]) <= tol("bf16")
     assert rel_err(outs["pairs"], outs["tokens"]) <= tol("bf16")
-    assert rel_err(outs["pairs_db"], outs["tokens"]) <= tol("bf16")
-
-
-@pytest.mark.parametrize("d,F", [(256, 384), (384, 256), (1024, 512)])
-def test_double_buffered_pairs_gelu_many_tiles_per_pair(d, F):
-    """The double-buffered SM-pair kernel alternates its two accumulators from
-    tile to tile: with far more tiles than SM pairs every pair runs many tiles
-    in both accumulators (GELU up, plain down; d = 384 leaves a half-empty
-    last feature tile)."""
-    counts = [700, 513, 64, 1, 900, 0, 333, 1500, 257, 16, 17, 255]
-    B.set_ffn_tiling("pairs_db")
-    try:
-        check(counts, d, F, "gelu_tanh", "bf16", seed=d + F + 7)
-    finally:
-        B.set_ffn_tiling("auto")

@@ -50,25 +50,7 @@ static_assert(kPrSmemBytes <= 227 * 1024, "pair kernel shared memory");
 template <int EPI>
 __host__ __device__ constexpr int pr_tile_features() { return EPI == EPI_SWIGLU ? 2 * kSwFM : 4 * kSwFM; }
 
-// ---------------------------------------------------------------- cluster / pair PTX
-__device__ __forceinline__ uint32_t cluster_cta_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of both CTAs: release this CTA's prior writes, wait for the peer's.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t smem_addr_in_cta(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
+// ---------------------------------------------------------------- pair PTX
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                : "memory");

@@ -103,6 +103,72 @@ __device__ __forceinline__ void load_x8(const float* p, float* v) {
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// One token's top-k, by one warp: k rounds of a warp-wide argmax over the
+// choosing scores v (ties -> lower expert id), then the renormalised weights
+// w_j = exp(g_j - g_max) / sum over the chosen of exp(g - g_max), g being the
+// softmax logits of the chosen experts (the max-shifted softmax restricted to
+// the k chosen). Expert n = lane + 32 m sits in slot m; taken marks experts
+// that may not be chosen (out of range). c_acc[m] += 1 for each chosen expert
+// of this lane (routing statistics). Writes idx_out[0..k) and w_out[0..k).
+template <int SLOTS>
+__device__ __forceinline__ void topk_renorm(const float* g, const float* v, bool* taken, int k, int lane,
+                                            int32_t* __restrict__ idx_out, float* __restrict__ w_out, float* c_acc) {
+  float sel_v[SLOTS];
+  int sel_i[SLOTS];
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) { sel_v[m] = -INFINITY; sel_i[m] = 0; }
+  float top = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int m = 0; m < SLOTS; ++m) {
+      const int n = lane + 32 * m;
+      if (!taken[m] && (v[m] > bv || (v[m] == bv && n < bi))) { bv = v[m]; bi = n; }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    // the winner's softmax logit (its score unless the bias only chooses)
+    float gw = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < SLOTS; ++m)
+      if ((bi >> 5) == m) gw = g[m];
+    gw = __shfl_sync(0xffffffffu, gw, bi & 31);
+    top = (j == 0) ? gw : fmaxf(top, gw);
+#pragma unroll
+    for (int m = 0; m < SLOTS; ++m) {
+      if (bi == lane + 32 * m) {
+        taken[m] = true;
+        c_acc[m] += 1.f;
+      }
+      if ((j & 31) == lane && (j >> 5) == m) { sel_v[m] = gw; sel_i[m] = bi; }
+    }
+  }
+  float part = 0.f;
+  float ex[SLOTS];
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const int j = lane + 32 * m;
+    ex[m] = (j < k) ? expf(sel_v[m] - top) : 0.f;
+    part += ex[m];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+  const float inv = 1.f / part;
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const int j = lane + 32 * m;
+    if (j < k) {
+      idx_out[j] = sel_i[m];
+      w_out[j] = ex[m] * inv;
+    }
+  }
+}
+
 template <int EG, int EPT, int TPT, typename TX, int THR = kRouteThreads>
 __global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, const float* __restrict__ wg,
                                                               const float* __restrict__ bias, int T, int d, int N,
@@ -276,62 +342,8 @@ __global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, co
       v[m] = (n < N) ? g[m] + bsel[m] : -INFINITY;
       taken[m] = (n >= N);
     }
-    if (topk_idx != nullptr) {   // top-k choice and its renormalised weights
-      float sel_v[SLOTS];
-      int sel_i[SLOTS];
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m) { sel_v[m] = -INFINITY; sel_i[m] = 0; }
-      float top = 0.f;
-      for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7FFFFFFF;
-#pragma unroll
-        for (int m = 0; m < SLOTS; ++m) {
-          const int n = lane + 32 * m;
-          if (!taken[m] && (v[m] > bv || (v[m] == bv && n < bi))) { bv = v[m]; bi = n; }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-          if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        // the winner's softmax logit (its score unless the bias only chooses)
-        float gw = -INFINITY;
-#pragma unroll
-        for (int m = 0; m < SLOTS; ++m)
-          if ((bi >> 5) == m) gw = g[m];
-        gw = __shfl_sync(0xffffffffu, gw, bi & 31);
-        top = (j == 0) ? gw : fmaxf(top, gw);
-#pragma unroll
-        for (int m = 0; m < SLOTS; ++m) {
-          if (bi == lane + 32 * m) {
-            taken[m] = true;
-            c_acc[m] += 1.f;
-          }
-          if ((j & 31) == lane && (j >> 5) == m) { sel_v[m] = gw; sel_i[m] = bi; }
-        }
-      }
-      float part = 0.f;
-      float ex[SLOTS];
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m) {
-        const int j = lane + 32 * m;
-        ex[m] = (j < k) ? expf(sel_v[m] - top) : 0.f;
-        part += ex[m];
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-      const float inv = 1.f / part;
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m) {
-        const int j = lane + 32 * m;
-        if (j < k) {
-          topk_idx[t * k + j] = sel_i[m];
-          topk_w[t * k + j] = ex[m] * inv;
-        }
-      }
-    }
+    if (topk_idx != nullptr)   // top-k choice and its renormalised weights
+      topk_renorm<SLOTS>(g, v, taken, k, lane, topk_idx + t * k, topk_w + t * k, c_acc);
     if (want_stats || probs_out != nullptr) {   // full softmax over the N experts
       float gmax = -INFINITY;
 #pragma unroll
@@ -387,6 +399,139 @@ __global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, co
     for (int w = 0; w < THR / 32; ++w) ts += srow[w * SW + 2 * NP];
     out[2 * N] = ts;
   }
+}
+
+// Small batches (decode): each logit chain is d sequential FMAs, so the time
+// floor is d FMA latencies whatever the parallelism, and the batch is too
+// small to fill the GPU with chains. This kernel trims the per-step work of a
+// chain: one CTA holds TC tokens and all N experts (N = NP); its TC x rows
+// (contiguous in memory) arrive in shared memory by one bulk copy, and W_g
+// streams through a ring of S slices of BK whole rows (each slice contiguous
+// in memory, one bulk copy) on mbarriers, every copy issued by one thread, so
+// the chains' threads issue no copies. Each thread owns the chains of two
+// neighbouring experts (thread (t, p) = (tid / (NP/2), tid % (NP/2)), experts
+// 2p and 2p + 1): a step is one 8-byte shared load of W_g[i, 2p..2p+1], one
+// widened x value (eight per 16-byte broadcast load) and two independent
+// FMAs. Same arithmetic as route_kernel (each chain over i in index order,
+// one fp32 bias add), so the routing is identical bit for bit; statistics and
+// probability outputs are route_kernel's. Needs N = NP and d a multiple of
+// BK. Every wait on a copy is bounded: on a timeout the CTA records
+// MOE_ERR_TIMEOUT, lets its copies in flight land and writes nothing.
+template <int NP>
+struct RouteSmallCfg {
+  static constexpr int BK = 64;
+  static constexpr int WBYTES = BK * NP * 4;
+  static constexpr int SFIT = (96 * 1024) / WBYTES;
+  static constexpr int STAGES = SFIT < 3 ? 3 : (SFIT > 8 ? 8 : SFIT);
+  // shared memory for TC tokens of d values of es bytes: ring, x rows, barriers
+  static size_t smem(int TC, int d, int es) {
+    return static_cast<size_t>(STAGES) * WBYTES + static_cast<size_t>(TC) * d * es + 8 * (STAGES + 1);
+  }
+};
+
+template <int NP, int TC, typename TX>
+__global__ void __launch_bounds__(TC * NP / 2) route_small_kernel(const TX* __restrict__ x,
+                                                                  const float* __restrict__ wg,
+                                                                  const float* __restrict__ bias, int T, int d,
+                                                                  int N, int k, int bias_select,
+                                                                  int32_t* __restrict__ topk_idx,
+                                                                  float* __restrict__ topk_w,
+                                                                  unsigned long long timeout_ns) {
+  using C = RouteSmallCfg<NP>;
+  constexpr int NPH = NP / 2;                     // threads per token
+  constexpr int THR = TC * NPH, BK = C::BK, S = C::STAGES;
+  constexpr int SLOTS = NP / 32;
+  static_assert(NP % 64 == 0 && THR / 32 >= TC, "one warp per token for the top-k");
+  extern __shared__ __align__(16) uint8_t rs_smem[];
+  float* ws = reinterpret_cast<float*>(rs_smem);                                  // [S][BK][NP]
+  TX* xs = reinterpret_cast<TX*>(rs_smem + static_cast<size_t>(S) * C::WBYTES);  // [TC][d]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xs) +
+                                               static_cast<size_t>(TC) * d * sizeof(TX));   // full[S], x
+  const int tid = threadIdx.x;
+  const int tl = tid / NPH, n = 2 * (tid % NPH);  // experts n, n + 1
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * TC;
+  const int KB = d / BK;
+  const int rows = static_cast<int>(min(static_cast<int64_t>(TC), static_cast<int64_t>(T) - t0));
+
+  if (tid == 0) {
+    for (int s = 0; s <= S; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  int issued = 0;
+  if (tid == 0) {
+    // rows past T are never copied: their chains compute garbage nobody reads
+    const uint32_t xb = static_cast<uint32_t>(rows) * d * sizeof(TX);
+    mbar_arrive_expect_tx(smem_addr(&bars[S]), xb);
+    bulk_load(smem_addr(xs), x + t0 * d, xb, smem_addr(&bars[S]));
+    for (; issued < S - 1 && issued < KB; ++issued) {
+      mbar_arrive_expect_tx(smem_addr(&bars[issued]), C::WBYTES);
+      bulk_load(smem_addr(ws + issued * BK * NP), wg + static_cast<int64_t>(issued) * BK * NP, C::WBYTES,
+                smem_addr(&bars[issued]));
+    }
+  }
+  bool ok = mbar_wait_bounded(smem_addr(&bars[S]), 0u, nullptr, timeout_ns);
+
+  float acc0 = 0.f, acc1 = 0.f;
+  const TX* xr = xs + static_cast<int64_t>(tl) * d;
+  int kb = 0;
+  for (; kb < KB; ++kb) {
+    ok = ok && mbar_wait_bounded(smem_addr(&bars[kb % S]), static_cast<uint32_t>((kb / S) & 1), nullptr, timeout_ns);
+    // uniform decision; every thread is done with slice kb - 1, so its slot may be refilled
+    if (__syncthreads_or(!ok)) break;
+    if (tid == 0 && issued < KB) {
+      const int s = issued % S;
+      mbar_arrive_expect_tx(smem_addr(&bars[s]), C::WBYTES);
+      bulk_load(smem_addr(ws + s * BK * NP), wg + static_cast<int64_t>(issued) * BK * NP, C::WBYTES,
+                smem_addr(&bars[s]));
+      ++issued;
+    }
+    const float2* wcol = reinterpret_cast<const float2*>(ws + (kb % S) * BK * NP + n);
+    const TX* xk = xr + kb * BK;
+#pragma unroll
+    for (int g8 = 0; g8 < BK; g8 += 8) {
+      float xv[8];
+      load_x8(xk + g8, xv);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float2 w2 = wcol[(g8 + u) * NPH];
+        acc0 = fmaf(xv[u], w2.x, acc0);
+        acc1 = fmaf(xv[u], w2.y, acc1);
+      }
+    }
+  }
+  if (kb < KB) {
+    // gave up: let every copy in flight land before the CTA exits, write nothing
+    if (tid == 0) {
+      for (int i = kb; i < issued; ++i)
+        mbar_wait_bounded(smem_addr(&bars[i % S]), static_cast<uint32_t>((i / S) & 1), nullptr, timeout_ns);
+    }
+    return;
+  }
+  __syncthreads();
+
+  // logits (+ bias, unless it only chooses) -> lg[token][n]
+  float* lg = reinterpret_cast<float*>(rs_smem);                                  // [TC][NP + 1]
+  const bool add_bias = bias != nullptr && !bias_select;
+  lg[tl * (NP + 1) + n] = acc0 + (add_bias ? bias[n] : 0.f);
+  lg[tl * (NP + 1) + n + 1] = acc1 + (add_bias ? bias[n + 1] : 0.f);
+  __syncthreads();
+
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp >= rows) return;
+  const int64_t t = t0 + warp;
+  float g[SLOTS], v[SLOTS], c_acc[SLOTS];
+  bool taken[SLOTS];
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const int e = lane + 32 * m;
+    const float bs = (bias != nullptr && bias_select) ? bias[e] : 0.f;
+    g[m] = lg[warp * (NP + 1) + e];
+    v[m] = g[m] + bs;
+    taken[m] = false;
+    c_acc[m] = 0.f;
+  }
+  topk_renorm<SLOTS>(g, v, taken, k, lane, topk_idx + t * k, topk_w + t * k, c_acc);
 }
 
 // Load statistics from the route kernel's per-CTA rows (one CTA, 256 threads,

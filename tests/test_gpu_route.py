@@ -43,6 +43,14 @@ CASES = [
     (6000, 512, 64, 2, "f32", True),
     (1000, 256, 64, 4, "bf16", False),     # 8 tokens per CTA
     (20000, 128, 8, 2, "bf16", True),      # 8 expert lanes, 128 tokens per CTA
+    # the small-batch kernel (64 or 128 experts, one CTA per token, whole-row W_g slices)
+    (1, 128, 64, 8, "bf16", False),
+    (31, 3584, 64, 8, "bf16", True),
+    (300, 384, 128, 8, "bf16", True),
+    (17, 256, 64, 2, "f32", True),
+    (600, 128, 64, 4, "bf16", False),      # past four CTAs per SM: the generic kernel again
+    (8192, 4096, 64, 2, "bf16", False),    # 56 tokens per CTA, 7 per thread
+    (16384, 512, 128, 8, "bf16", True),    # 112 tokens per CTA, 7 per thread
 ]
 
 
@@ -90,3 +98,28 @@ def test_route_repeatable():
     a = run_route(x_h, wg_h, b_h, w.k, w.dtype)
     b = run_route(x_h, wg_h, b_h, w.k, w.dtype)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("T,d,N,k,dtype,mode", [(1, 128, 64, 8, "bf16", "logits"), (40, 3584, 64, 8, "bf16", "select"),
+                                                (100, 256, 128, 8, "f32", "logits"),
+                                                (7, 1024, 128, 4, "bf16", "select")])
+def test_small_batch_kernel_equals_the_generic_kernel(T, d, N, k, dtype, mode):
+    """Asking for routing statistics takes the generic kernel; without them a
+    small batch takes the small-batch kernel. Both evaluate the same fp32
+    chains, so indices and weights agree bit for bit."""
+    w = S.Workload("route-small", T=T, d=d, N=N, k=k, F=64, act="swiglu", dtype=dtype, seed=T + d, zipf_s=1.2)
+    x_h, wg_h, b_h = S.x_all(w), S.gate_weight(w), S.gate_bias(w)
+    s = B.shape(T, d, N, k, 64, "swiglu", dtype)
+    x, wg, b = dev(x_h), dev(wg_h), dev(b_h)
+    outs = []
+    for stats in (False, True):
+        idx = new((T, k), "i32", fill=-7)
+        tw = new((T, k), "f32", fill=-1.0)
+        st = torch.empty(B.load_stats_len(N), dtype=torch.float32, device="cuda") if stats else None
+        ws = B.workspace(B.route_ex_workspace_size(s)) if stats else None
+        B.route_ex(s, x, wg, b, idx, tw, bias_mode=mode, load_stats=st, ws=ws)
+        assert B.get_error() == B.MOE_OK
+        outs.append((idx.cpu(), tw.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    r = oracle.route(x_h, wg_h, k, bias=b_h, bias_mode=mode)
+    np.testing.assert_array_equal(outs[0][0].numpy(), r["topk_idx"])

@@ -365,16 +365,24 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
         else:
             B.route(s, x, wg, bias, idx, tw)
 
+    # token choice: the grouping writes the permuted copy x_perm and the grouped GEMM reads it (the
+    # path moe_forward takes); --gather: indices only, the first GEMM gathers the rows of x through perm
+    gather = not ec and w.dtype == "bf16" and args.gather
+    xp_arg = None if gather else xp
+
     def stage_permute():
         if ec:
             B.gather_rows(s, inv_ec, w.N, A, x, xp)
         elif cf is None:
-            B.permute(s, idx, x, counts, offsets, perm, inv, xp, ws)
+            B.permute(s, idx, x, counts, offsets, perm, inv, xp_arg, ws)
         else:
-            B.permute_capacity(s, idx, x, cf, counts, offsets, perm, inv, xp, ws, dropped=dropped)
+            B.permute_capacity(s, idx, x, cf, counts, offsets, perm, inv, xp_arg, ws, dropped=dropped)
 
     def stage_ffn():
-        B.grouped_ffn(s_rows, xp, offsets, WG, WU, WD, yp, ws)
+        if gather:
+            B.grouped_ffn_gather(s_rows, x, perm, offsets, WG, WU, WD, yp, ws)
+        else:
+            B.grouped_ffn(s_rows, xp, offsets, WG, WU, WD, yp, ws)
 
     def stage_combine():
         if ec:
@@ -579,7 +587,7 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
                           f"whose experts lie in a {len(cpu_used)}-expert subset; {secs:.1f} s")}
     stage_ms = {"route": float(np.median(stage[:, 0])), "permute": float(np.median(stage[:, 1])),
                 "grouped_ffn": ffn_ms, "combine": float(np.median(stage[:, 3]))}
-    return dict(w=w, C=C, ec=ec, cf=cf, step_ms=step_ms, ffn_ms=ffn_ms, stage_ms=stage_ms, cnt=cnt,
+    return dict(w=w, C=C, ec=ec, cf=cf, gather=gather, step_ms=step_ms, ffn_ms=ffn_ms, stage_ms=stage_ms, cnt=cnt,
                 ffn_flops=ffn_flops, roof=roof, cpu=cpu, e2e=e2e, clocks=clk.summary(),
                 routing_stats=routing_stats, dropped=int(dropped.item()) if cf is not None else 0,
                 graphs=graphs is not None, fwd_bytes=fwd_bytes, P=P)
@@ -608,6 +616,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gather", action="store_true",
+                    help="grouping without x_perm; the grouped GEMM gathers token rows through perm")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode-shaped sub-record that follows the headline workload")
     ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs"],
@@ -679,6 +689,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "d_ff": w.F, "act": w.act,
                    "gate": "fp32", "ffn_tiling": args.ffn_tiling, "capacity_factor": cf,
+                   "token_rows": "gathered by the grouped GEMM through perm" if r["gather"] else "x_perm copy",
                    "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write, then 2 x 126 MB read of another buffer); expert weights also exceed L2"},
         "timing": ("median over steps; every stage is a CUDA-graph replay between CUDA events on the stream"
@@ -690,9 +701,9 @@ def main():
         "routing_stats": r["routing_stats"], "dropped_assignments": r["dropped"],
         "roofline": r["roof"], "route_roofline": route_roofline(r, fma), "fma_peak": fma,
         "cpu_baseline": r["cpu"], "e2e": r["e2e"],
-        # token choice: route 1 + permute 4 (hist, scan, rank, copy) + grouped FFN 2 + combine 1;
-        # expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
-        "gpu_launches": (6 if ec else 8) * args.steps,
+        # token choice: route 1 + grouping 3 (hist, scan, rank) + row copy 1 unless gathered + grouped FFN 2
+        # + combine 1; expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
+        "gpu_launches": (6 if ec else (7 if r["gather"] else 8)) * args.steps,
         "clocks": r["clocks"],
         "decode": dec,
         "kernel_source": kernel_source_hash(),

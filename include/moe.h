@@ -116,6 +116,8 @@ size_t moe_route_ex_workspace_size(const moe_shape *s);
  *   perm[row] = t,  inv_perm[f] = row,  x_perm[row,:] = x[t,:]
  * topk_idx [T,k]; x [T,d]; x_perm [T*k, d] (dtype of x). Bit-exact and
  * deterministic. ws: at least moe_permute_workspace_size(s) bytes.
+ * x_perm may be NULL (x is then not read): counts, offsets, perm and
+ * inv_perm only, for moe_grouped_ffn_gather, which loads the rows itself.
  * An index outside [0,N) records MOE_ERR_CORRUPT.
  */
 moe_status moe_permute(const moe_shape *s, const int32_t *topk_idx, const void *x,
@@ -142,6 +144,24 @@ moe_status moe_permute(const moe_shape *s, const int32_t *topk_idx, const void *
 moe_status moe_grouped_ffn(const moe_shape *s, const void *x_perm, const int32_t *offsets,
                            const void *w_gate, const void *w_up, const void *w_down,
                            void *y_perm, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * moe_grouped_ffn with the first GEMM's rows taken from the unpermuted tokens:
+ * row r of expert e's block is token perm[r], loaded by the GEMM's TMA
+ * through the permutation ("MoE显存与计算开销四阶段手算指南" section 4.3 notes
+ * what non-contiguous expert inputs cost; here the rows are gathered by the
+ * tile loads, so the contiguous x_perm is never written or read). x [T,d]
+ * bf16 and perm [A] as from moe_permute (x_perm may be NULL there); other
+ * arguments, the result and the workspace as moe_grouped_ffn. bf16 only
+ * (MOE_ERR_UNSUPPORTED for fp32). Bit-identical to moe_grouped_ffn on the
+ * copy, and saves the T*k x d x_perm buffer and its copy, but is slower on
+ * B300 (worked example: 5.1 ms against 3.7-3.8 ms for the grouped FFN; the
+ * per-row gathers slow the weight stream), so moe_forward does not use it.
+ */
+moe_status moe_grouped_ffn_gather(const moe_shape *s, const void *x, const int32_t *perm,
+                                  const int32_t *offsets, const void *w_gate, const void *w_up,
+                                  const void *w_down, void *y_perm, void *ws, size_t ws_bytes,
+                                  void *stream);
 
 /*
  * Weighted combine back to token order: "MoE显存与计算开销四阶段手算指南"
@@ -174,8 +194,9 @@ moe_status moe_forward(const moe_shape *s, const void *x, const float *w_g, cons
  * its earliest assignments in flat order t*k + j. Outputs as moe_permute,
  * except: counts / offsets describe the kept rows (offsets[N] <= T*k),
  * inv_perm[f] = -2 for a dropped assignment, and *dropped (optional, int32)
- * receives the number of dropped assignments. moe_grouped_ffn and
- * moe_combine accept these directly (a dropped assignment adds nothing to
+ * receives the number of dropped assignments; x_perm may be NULL as for
+ * moe_permute. moe_grouped_ffn, moe_grouped_ffn_gather and moe_combine
+ * accept these directly (a dropped assignment adds nothing to
  * the token's output; kept gate weights are not renormalised).
  */
 moe_status moe_permute_capacity(const moe_shape *s, const int32_t *topk_idx, const void *x,

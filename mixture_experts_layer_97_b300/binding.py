@@ -55,6 +55,7 @@ SIGNATURES = {
     "moe_route": (I32, [SP, P, P, P, P, P, P]),
     "moe_permute": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_grouped_ffn": (I32, [SP, P, P, P, P, P, P, P, SZ, P]),
+    "moe_grouped_ffn_gather": (I32, [SP, P, P, P, P, P, P, P, P, SZ, P]),
     "moe_permute_noalloc": (I32, [SP, P, P, P, P, P, P, P, P]),
     "moe_permute_capacity": (I32, [SP, P, P, ctypes.c_double, P, P, P, P, P, P, P, SZ, P]),
     "moe_forward_capacity": (I32, [SP, ctypes.c_double, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]),
@@ -276,6 +277,12 @@ def ep_ungroup(local_src, y_local, y_recv, dtype, stream=None):
     rows, d = int(y_local.shape[0]), int(y_local.shape[1])
     _check(lib().moe_ep_ungroup(rows, d, DTYPE[dtype], _ptr(local_src), _ptr(y_local), _ptr(y_recv),
                                 _stream(stream)), "moe_ep_ungroup")
+
+
+def grouped_ffn_gather(s, x, perm, offsets, w_gate, w_up, w_down, y_perm, ws, stream=None):
+    _check(lib().moe_grouped_ffn_gather(ctypes.byref(s), _ptr(x), _ptr(perm), _ptr(offsets), _ptr(w_gate),
+                                        _ptr(w_up), _ptr(w_down), _ptr(y_perm), _ptr(ws),
+                                        ws.numel() if ws is not None else 0, _stream(stream)), "moe_grouped_ffn_gather")
 
 
 def combine(s, y_perm, inv_perm, topk_w, out, stream=None):

@@ -120,6 +120,40 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// TMA gather: rows r0..r3 (each box-width columns from column x) of a 2-D
+// tensor whose map has a box one row high, written to shared memory as four
+// consecutive rows (swizzled by the map's mode); completion counted in bytes
+// on the mbarrier. Rows outside the tensor read the fill value.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int r0, int r1,
+                                            int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+// The same for one CTA of an SM pair, completion counted on the even CTA's
+// mbarrier (bar_cluster: a shared::cluster address).
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar_cluster)
+      : "memory");
+}
+
+// Token ids of the four rows a lane gathers: rows base + 4 q + j of the
+// permuted order for j < 4, valid while below `valid` (else the first row's
+// token, a real row whose result is never stored).
+__device__ __forceinline__ int4 gather_rows4(const int32_t* __restrict__ perm, int base, int q, int valid) {
+  const int r = 4 * q;
+  const int f = perm[base];
+  return make_int4(r < valid ? perm[base + r] : f, r + 1 < valid ? perm[base + r + 1] : f,
+                   r + 2 < valid ? perm[base + r + 2] : f, r + 3 < valid ? perm[base + r + 3] : f);
+}
+
 // Contiguous bulk copy global -> shared (no tensor map): both addresses 16-byte
 // aligned, bytes a multiple of 16; completion counted in bytes on the mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

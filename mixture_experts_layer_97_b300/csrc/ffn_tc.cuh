@@ -7,7 +7,11 @@
 //
 //   warp 0     TMA producer: A tile (128 permuted rows x 64 K) and B tile
 //              (BN weight rows x 64 K) per stage, 128-byte swizzle, into an
-//              S-stage shared-memory ring guarded by full/empty mbarriers
+//              S-stage shared-memory ring guarded by full/empty mbarriers.
+//              With GATHER the A rows come straight from the unpermuted
+//              tokens x through the permutation (perm[row] = token): each
+//              lane of the warp gathers four of the tile's rows per stage
+//              (TMA tile::gather4), so no permuted copy of x is needed
 //   warp 1     allocates 2*BN TMEM columns (two fp32 accumulators), one
 //              thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 -> fp32)
 //              and commits stages back to the producer
@@ -44,12 +48,12 @@ struct TcCfg {
                                        2 * 257 * sizeof(int) + 16;
 };
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool GATHER = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                            const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets, int N,
                            int rows_total, int K, int Nout, __nv_bfloat16* __restrict__ out, int ldo,
-                           unsigned long long timeout_ns) {
+                           unsigned long long timeout_ns, const int32_t* __restrict__ perm) {
   using C = TcCfg<BN>;
   constexpr int S = C::kStages;
   constexpr int HB = (EPI == EPI_SWIGLU) ? BN / 2 : BN;  // weight rows per TMA box = output columns
@@ -109,8 +113,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const long long total = bad ? 0 : static_cast<long long>(s_pre[N]) * n_tiles;
   const int KB = K / kTcBK;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
+  if (warp == 0 && (GATHER || lane == 0)) {
+    // ---------------- TMA producer (lane 0 waits and loads the weights; with GATHER every lane
+    // also gathers four rows of the A tile)
     int s = 0;
     uint32_t ph = 0;
     long long issued = 0;
@@ -118,23 +123,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (long long id = blockIdx.x; id < total && ok; id += gridDim.x) {
       const TileInfo ti = decode_tile(id, s_off, s_pre, N, n_tiles, kTcBM);
       const int brow = ti.e * Nout + ti.nt * HB;
+      int4 tok = make_int4(0, 0, 0, 0);
+      if constexpr (GATHER) tok = gather_rows4(perm, ti.row0, lane, ti.rows);
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_bounded(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag, timeout_ns)) {
+        bool go = lane != 0 || mbar_wait_bounded(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag, timeout_ns);
+        if constexpr (GATHER) go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) {
           ok = false;
           break;
         }
         const uint32_t fb = smem_addr(&full_bar[s]);
-        mbar_arrive_expect_tx(fb, C::kStageBytes);
         const uint32_t sa = smem_addr(stage_a + s * C::kABytes);
         const uint32_t sb = smem_addr(stage_b + s * C::kBBytes);
-        tma_load_2d(sa, &tmA, fb, kb * kTcBK, ti.row0);
-        tma_load_2d(sb, &tmB0, fb, kb * kTcBK, brow);
-        if (EPI == EPI_SWIGLU) tma_load_2d(sb + HB * kTcBK * 2, &tmB1, fb, kb * kTcBK, brow);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          if (!GATHER) tma_load_2d(sa, &tmA, fb, kb * kTcBK, ti.row0);
+          tma_load_2d(sb, &tmB0, fb, kb * kTcBK, brow);
+          if (EPI == EPI_SWIGLU) tma_load_2d(sb + HB * kTcBK * 2, &tmB1, fb, kb * kTcBK, brow);
+        }
+        if constexpr (GATHER) {
+          __syncwarp();
+          tma_gather4(sa + lane * (4 * kTcBK * 2), &tmA, fb, kb * kTcBK, tok.x, tok.y, tok.z, tok.w);
+        }
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       // let every copy still in flight land before the CTA exits
       const long long first = issued > S ? issued - S : 0;
       for (long long i = first; i < issued; ++i)

@@ -19,6 +19,10 @@
 // balanced per expert, multiples of 16); CTA r holds tokens
 // [r nt / 2, (r + 1) nt / 2) of the tile.
 //
+// With GATHER (the first GEMM of the layer) the token rows come straight from
+// the unpermuted tokens x through the permutation (perm[row] = token): lanes
+// of warp 0 gather four rows each per stage (TMA tile::gather4).
+//
 // Roles (both CTAs): warp 0 TMA producer for the CTA's own shared memory,
 // warp 1 TMEM (allocated by both CTAs together) and, in the even CTA only,
 // the MMA issuer; warps 2-9 epilogue on the CTA's own TMEM (its 128 weight
@@ -100,12 +104,12 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
-template <int EPI>
+template <int EPI, bool GATHER = false>
 __global__ void __launch_bounds__(kSwThreads, 1)
     grouped_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                                 const __grid_constant__ CUtensorMap tmX, const int32_t* __restrict__ offsets, int N,
                                 int rows_total, int K, int Nout, __nv_bfloat16* __restrict__ out, int ldo,
-                                unsigned long long timeout_ns) {
+                                unsigned long long timeout_ns, const int32_t* __restrict__ perm) {
   constexpr int S = kPrStages;
   constexpr int OFP = pr_tile_features<EPI>();      // features per pair tile
   constexpr int OFC = OFP / 2;                      // features of this CTA
@@ -170,8 +174,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   const int KB = K / kTcBK;
   const long long pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer (each CTA fills its own shared memory)
+  if (warp == 0 && (GATHER || lane == 0)) {
+    // ---------------- TMA producer (each CTA fills its own shared memory; lane 0 waits and loads
+    // the weights, and with GATHER the first lanes gather four token rows each)
     int s = 0;
     uint32_t ph = 0;
     long long issued = 0;
@@ -183,25 +188,43 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const int half = t.nt >> 1;                               // token rows per CTA
       const int r0 = t.row0 + static_cast<int>(rank) * half;
       const int nbox = (half + kSwBox - 1) / kSwBox;
-      const uint32_t tx_pair = 2u * (kPrABytes + nbox * kSwBox * kPrRowBytes);
+      const int ngat = (half + 3) / 4;                          // gathers of four rows (GATHER)
+      const uint32_t tx_pair =
+          2u * (kPrABytes + (GATHER ? ngat * 4 * kPrRowBytes : nbox * kSwBox * kPrRowBytes));
+      int4 tok = make_int4(0, 0, 0, 0);
+      if constexpr (GATHER) {
+        // this CTA's valid rows of the tile: [rank * half, rank * half + half) clipped to t.rows
+        const int valid = min(half, max(0, t.rows - static_cast<int>(rank) * half));
+        tok = valid > 0 ? gather_rows4(perm, r0, lane, valid) : gather_rows4(perm, t.row0, 0, 1);
+      }
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_bounded(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag, timeout_ns)) {
+        bool go = lane != 0 || mbar_wait_bounded(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag, timeout_ns);
+        if constexpr (GATHER) go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) {
           ok = false;
           break;
         }
         const uint32_t fb = smem_addr_in_cta(smem_addr(&full_bar[s]), 0);
-        if (leader) mbar_arrive_expect_tx(smem_addr(&full_bar[s]), tx_pair);
         const uint32_t sa = smem_addr(stage_a + s * kPrABytes);
         const uint32_t sb = smem_addr(stage_b + s * kPrBBytes);
-        tma_load_2d_pair(sa, &tmW0, fb, kb * kTcBK, w0row);
-        tma_load_2d_pair(sa + kPrWBytes, (EPI == EPI_SWIGLU) ? &tmW1 : &tmW0, fb, kb * kTcBK, w1row);
-        for (int b = 0; b < nbox; ++b)
-          tma_load_2d_pair(sb + b * kSwBox * kPrRowBytes, &tmX, fb, kb * kTcBK, r0 + b * kSwBox);
+        if (lane == 0) {
+          if (leader) mbar_arrive_expect_tx(smem_addr(&full_bar[s]), tx_pair);
+          tma_load_2d_pair(sa, &tmW0, fb, kb * kTcBK, w0row);
+          tma_load_2d_pair(sa + kPrWBytes, (EPI == EPI_SWIGLU) ? &tmW1 : &tmW0, fb, kb * kTcBK, w1row);
+          if (!GATHER)
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d_pair(sb + b * kSwBox * kPrRowBytes, &tmX, fb, kb * kTcBK, r0 + b * kSwBox);
+        }
+        if constexpr (GATHER) {
+          __syncwarp();
+          if (lane < ngat)
+            tma_gather4_pair(sb + lane * (4 * kPrRowBytes), &tmX, fb, kb * kTcBK, tok.x, tok.y, tok.z, tok.w);
+        }
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
       }
     }
-    if (!ok && leader) {
+    if (!ok && leader && lane == 0) {
       // let the copies still in flight (both CTAs') land before the CTAs leave
       const long long first = issued > S ? issued - S : 0;
       for (long long i = first; i < issued; ++i)

@@ -122,12 +122,16 @@ __device__ __forceinline__ void sw_store_transposed(const uint32_t* v, uint8_t* 
   __syncwarp();
 }
 
-template <int EPI, int BK>
+// With GATHER the token rows come straight from the unpermuted tokens x
+// through the permutation (perm[row] = token), four rows per lane of warp 0
+// per stage (TMA tile::gather4); the map of x then has a box one row high.
+template <int EPI, int BK, bool GATHER = false>
 __global__ void __launch_bounds__(kSwThreads, 1)
     grouped_gemm_tc_swap_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                                 const __grid_constant__ CUtensorMap tmX, const int32_t* __restrict__ offsets, int N,
                                 int rows_total, int K, int Nout, __nv_bfloat16* __restrict__ out, int ldo,
-                                unsigned long long timeout_ns) {
+                                unsigned long long timeout_ns, const int32_t* __restrict__ perm) {
+  static_assert(!GATHER || BK == 64, "gathered rows are 128-byte swizzled");
   using C = SwCfg<BK>;
   constexpr int S = C::kStages;
   constexpr int OF = sw_tile_features<EPI>();
@@ -186,8 +190,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   const long long total = bad ? 0 : static_cast<long long>(s_pre[N]) * n_ftiles;
   const int KB = K / BK;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
+  if (warp == 0 && (GATHER || lane == 0)) {
+    // ---------------- TMA producer (lane 0 waits and loads the weights; with GATHER the lanes
+    // gather four token rows each, twice for tiles of more than 128 rows)
     int s = 0;
     uint32_t ph = 0;
     long long issued = 0;
@@ -198,25 +203,43 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       const int w0row = t.e * Nout + t.fi * OF;
       const int w1row = (EPI == EPI_SWIGLU) ? w0row : w0row + kSwFM;
       const int nbox = (t.nt + kSwBox - 1) / kSwBox;
-      const uint32_t tx_bytes = C::kABytes + nbox * kSwBox * C::kRowBytes;
+      const int ngat = (t.nt + 3) / 4;
+      const uint32_t tx_bytes = C::kABytes + (GATHER ? ngat * 4 * C::kRowBytes : nbox * kSwBox * C::kRowBytes);
+      int4 tok0 = make_int4(0, 0, 0, 0), tok1 = tok0;
+      if constexpr (GATHER) {
+        tok0 = gather_rows4(perm, t.row0, lane, t.rows);
+        tok1 = gather_rows4(perm, t.row0, lane + 32, t.rows);
+      }
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait_bounded(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag, timeout_ns)) {
+        bool go = lane != 0 || mbar_wait_bounded(smem_addr(&empty_bar[s]), ph ^ 1u, abort_flag, timeout_ns);
+        if constexpr (GATHER) go = __shfl_sync(0xffffffffu, go, 0);
+        if (!go) {
           ok = false;
           break;
         }
         const uint32_t fb = smem_addr(&full_bar[s]);
-        mbar_arrive_expect_tx(fb, tx_bytes);
         const uint32_t sa = smem_addr(stage_a + s * C::kABytes);
         const uint32_t sb = smem_addr(stage_b + s * C::kBBytes);
-        tma_load_2d(sa, &tmW0, fb, kb * BK, w0row);
-        tma_load_2d(sa + C::kWBytes, (EPI == EPI_SWIGLU) ? &tmW1 : &tmW0, fb, kb * BK, w1row);
-        for (int b = 0; b < nbox; ++b)
-          tma_load_2d(sb + b * kSwBox * C::kRowBytes, &tmX, fb, kb * BK, t.row0 + b * kSwBox);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, tx_bytes);
+          tma_load_2d(sa, &tmW0, fb, kb * BK, w0row);
+          tma_load_2d(sa + C::kWBytes, (EPI == EPI_SWIGLU) ? &tmW1 : &tmW0, fb, kb * BK, w1row);
+          if (!GATHER)
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(sb + b * kSwBox * C::kRowBytes, &tmX, fb, kb * BK, t.row0 + b * kSwBox);
+        }
+        if constexpr (GATHER) {
+          __syncwarp();
+          if (lane < ngat)
+            tma_gather4(sb + lane * (4 * C::kRowBytes), &tmX, fb, kb * BK, tok0.x, tok0.y, tok0.z, tok0.w);
+          if (lane + 32 < ngat)
+            tma_gather4(sb + (lane + 32) * (4 * C::kRowBytes), &tmX, fb, kb * BK, tok1.x, tok1.y, tok1.z, tok1.w);
+        }
         ++issued;
         if (++s == S) { s = 0; ph ^= 1u; }
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       // let every copy still in flight land before the CTA exits
       const long long first = issued > S ? issued - S : 0;
       for (long long i = first; i < issued; ++i)

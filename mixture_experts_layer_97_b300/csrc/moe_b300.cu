@@ -292,6 +292,8 @@ moe_status launch_row_copy(const moe_shape* s, const int32_t* inv, const void* x
 }
 
 
+// x_perm == nullptr: counts, offsets, perm and inv_perm only (the grouped GEMM
+// then gathers the token rows of x through perm itself).
 moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, int32_t* counts, int32_t* offsets,
                         int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, cudaStream_t st,
                         long long capacity = kNoCapacity, int32_t* dropped = nullptr) {
@@ -307,6 +309,7 @@ moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, i
     permute_rank_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, hist, offsets, s->T, s->N, s->k,
                                                                             capacity, perm, inv_perm, dropped);
     if (launched() != MOE_OK) return MOE_ERR_CUDA;
+    if (x_perm == nullptr) return MOE_OK;
     return launch_row_copy(s, inv_perm, x, s->k, n_assign(s), x_perm, st);
   }
   return MOE_OK;
@@ -365,15 +368,31 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Where a grouped GEMM's token rows come from: the permuted rows a[A, K]
+// (perm == nullptr), or rows of the unpermuted a[a_rows, K] gathered through
+// perm (row -> token) by the kernel's loads.
+struct RowSource {
+  const void* a;
+  const int32_t* perm;
+  int64_t a_rows;
+};
+
+// The tensor map of a GEMM's token operand: box_rows-row boxes of permuted
+// rows, or one-row boxes of the unpermuted rows for gathering.
+bool make_row_map(CUtensorMap* m, const RowSource& src, int64_t A, int K, uint32_t box_rows) {
+  if (src.perm != nullptr) return make_map(m, src.a, static_cast<uint64_t>(src.a_rows), static_cast<uint64_t>(K), 1);
+  return make_map(m, src.a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), box_rows);
+}
+
 // One grouped GEMM on the tensor cores: out[rows, Nout-slices] for every expert.
 template <int BN, int EPI>
-moe_status launch_tc(const moe_shape* s, const void* a, int K, const void* b0, const void* b1, int Nout,
+moe_status launch_tc(const moe_shape* s, const RowSource& src, int K, const void* b0, const void* b1, int Nout,
                      const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
   using Cfg = TcCfg<BN>;
   constexpr int HB = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
   const int64_t A = n_assign(s);
   CUtensorMap ma, mb0, mb1;
-  if (!make_map(&ma, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kTcBM)) return MOE_ERR_CUDA;
+  if (!make_row_map(&ma, src, A, K, kTcBM)) return MOE_ERR_CUDA;
   const uint64_t brows = static_cast<uint64_t>(s->N) * Nout;
   if (!make_map(&mb0, b0, brows, static_cast<uint64_t>(K), HB)) return MOE_ERR_CUDA;
   if (EPI == EPI_SWIGLU) {
@@ -381,7 +400,7 @@ moe_status launch_tc(const moe_shape* s, const void* a, int K, const void* b0, c
   } else {
     mb1 = mb0;
   }
-  auto kern = grouped_gemm_tc_kernel<BN, EPI>;
+  auto kern = src.perm != nullptr ? grouped_gemm_tc_kernel<BN, EPI, true> : grouped_gemm_tc_kernel<BN, EPI, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmemBytes)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -389,20 +408,24 @@ moe_status launch_tc(const moe_shape* s, const void* a, int K, const void* b0, c
   const int64_t upper = ((A + kTcBM - 1) / kTcBM + s->N) * n_tiles;
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
   kern<<<grid, kTcThreads, Cfg::kSmemBytes, st>>>(ma, mb0, mb1, offsets, s->N, static_cast<int>(A), K, Nout,
-                                                  static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs);
+                                                  static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs, src.perm);
   return launched();
 }
 
 // The same grouped GEMM with weights as the MMA's M side and the tokens of
 // an expert as its N side (balanced token tiles, multiples of 16).
 template <int EPI, int BK>
-moe_status launch_tc_swap_bk(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
-                             const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+moe_status launch_tc_swap_bk(const moe_shape* s, const RowSource& src, int K, const void* w0, const void* w1,
+                             int Nout, const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
   using Cfg = SwCfg<BK>;
   constexpr int OF = sw_tile_features<EPI>();
   const int64_t A = n_assign(s);
   CUtensorMap mx, mw0, mw1;
-  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox, BK)) return MOE_ERR_CUDA;
+  if (src.perm != nullptr) {
+    if (!make_row_map(&mx, src, A, K, kSwBox)) return MOE_ERR_CUDA;
+  } else if (!make_map(&mx, src.a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox, BK)) {
+    return MOE_ERR_CUDA;
+  }
   const uint64_t wrows = static_cast<uint64_t>(s->N) * Nout;
   if (!make_map(&mw0, w0, wrows, static_cast<uint64_t>(K), kSwFM, BK)) return MOE_ERR_CUDA;
   if (EPI == EPI_SWIGLU) {
@@ -410,7 +433,8 @@ moe_status launch_tc_swap_bk(const moe_shape* s, const void* a, int K, const voi
   } else {
     mw1 = mw0;
   }
-  auto kern = grouped_gemm_tc_swap_kernel<EPI, BK>;
+  auto kern = src.perm != nullptr ? grouped_gemm_tc_swap_kernel<EPI, BK, true>
+                                  : grouped_gemm_tc_swap_kernel<EPI, BK, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(Cfg::kSmemBytes)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -418,19 +442,19 @@ moe_status launch_tc_swap_bk(const moe_shape* s, const void* a, int K, const voi
   const int64_t upper = ((A + kSwMaxNT - 1) / kSwMaxNT + s->N) * n_ftiles;
   const int grid = static_cast<int>(upper < num_sms() ? upper : num_sms());
   kern<<<grid, kSwThreads, Cfg::kSmemBytes, st>>>(mw0, mw1, mx, offsets, s->N, static_cast<int>(A), K, Nout,
-                                                  static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs);
+                                                  static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs, src.perm);
   return launched();
 }
 
 // The token-tile grouped GEMM on SM pairs: clusters of two CTAs sharing
 // each MMA (tcgen05 cta_group::2).
 template <int EPI>
-moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
+moe_status launch_tc_pair(const moe_shape* s, const RowSource& src, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
   constexpr int OFP = pr_tile_features<EPI>();
   const int64_t A = n_assign(s);
   CUtensorMap mx, mw0, mw1;
-  if (!make_map(&mx, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kSwBox, kTcBK)) return MOE_ERR_CUDA;
+  if (!make_row_map(&mx, src, A, K, kSwBox)) return MOE_ERR_CUDA;
   const uint64_t wrows = static_cast<uint64_t>(s->N) * Nout;
   if (!make_map(&mw0, w0, wrows, static_cast<uint64_t>(K), kSwFM, kTcBK)) return MOE_ERR_CUDA;
   if (EPI == EPI_SWIGLU) {
@@ -438,7 +462,7 @@ moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* 
   } else {
     mw1 = mw0;
   }
-  auto kern = grouped_gemm_tc_pair_kernel<EPI>;
+  auto kern = src.perm != nullptr ? grouped_gemm_tc_pair_kernel<EPI, true> : grouped_gemm_tc_pair_kernel<EPI, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPrSmemBytes)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -459,18 +483,18 @@ moe_status launch_tc_pair(const moe_shape* s, const void* a, int K, const void* 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kern, mw0, mw1, mx, offsets, s->N, static_cast<int>(A), K, Nout,
-                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs) != cudaSuccess)
+                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs, src.perm) != cudaSuccess)
     return MOE_ERR_CUDA;
   return launched();
 }
 
 template <int EPI>
-moe_status launch_tc_swap(const moe_shape* s, const void* a, int K, const void* w0, const void* w1, int Nout,
+moe_status launch_tc_swap(const moe_shape* s, const RowSource& src, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st, int mode) {
   // auto and "pairs" run token tiles on SM pairs, "tokens" on single SMs
   if (mode == MOE_TILING_TOKENS)
-    return launch_tc_swap_bk<EPI, kTcBK>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
-  return launch_tc_pair<EPI>(s, a, K, w0, w1, Nout, offsets, out, ldo, st);
+    return launch_tc_swap_bk<EPI, kTcBK>(s, src, K, w0, w1, Nout, offsets, out, ldo, st);
+  return launch_tc_pair<EPI>(s, src, K, w0, w1, Nout, offsets, out, ldo, st);
 }
 
 // K is the reduction length of the GEMM in question (d for the first, F for
@@ -496,35 +520,40 @@ moe_status launch_simt(const moe_shape* s, const void* a, int K, const void* b0,
   return launched();
 }
 
+// The grouped FFN: h = act(x W_1^T) per expert (the first GEMM), y = h W_2^T
+// (the second). src gives the first GEMM's token rows: the permuted rows
+// x_perm [A, d], or (bf16 only) the tokens x gathered through perm.
 // tiling: a moe_tiling value for this call, or -1 for the process-wide setting
 // (moe_set_ffn_tiling), read once per call so both GEMMs see the same mode.
-moe_status ffn_impl(const moe_shape* s, const void* x_perm, const int32_t* offsets, const void* w_gate,
+moe_status ffn_impl(const moe_shape* s, const RowSource& src, const int32_t* offsets, const void* w_gate,
                     const void* w_up, const void* w_down, void* y_perm, void* ws, cudaStream_t st,
                     int tiling = -1) {
   if (n_assign(s) == 0) return MOE_OK;
   const int d = s->d, F = s->d_ff;
   const int mode = tiling >= 0 ? tiling : g_ffn_tiling.load(std::memory_order_relaxed);
   void* h = ws;
+  const RowSource hs{h, nullptr, 0};
   moe_status r;
   if (s->dtype == MOE_BF16) {
     if (use_token_tiles(s, d, mode))
       r = (s->act == MOE_SWIGLU)
-              ? launch_tc_swap<EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st, mode)
-              : launch_tc_swap<EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st, mode);
+              ? launch_tc_swap<EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st, mode)
+              : launch_tc_swap<EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st, mode);
     else if (s->act == MOE_SWIGLU)
-      r = (F % 128 == 0) ? launch_tc<256, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
-                         : launch_tc<128, EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st);
+      r = (F % 128 == 0) ? launch_tc<256, EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st)
+                         : launch_tc<128, EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st);
     else
-      r = (F % 256 == 0) ? launch_tc<256, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st)
-                         : launch_tc<128, EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
+      r = (F % 256 == 0) ? launch_tc<256, EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st)
+                         : launch_tc<128, EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st);
     if (r != MOE_OK) return r;
     if (use_token_tiles(s, F, mode))
-      return launch_tc_swap<EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st, mode);
-    return (d % 256 == 0) ? launch_tc<256, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st)
-                          : launch_tc<128, EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
+      return launch_tc_swap<EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st, mode);
+    return (d % 256 == 0) ? launch_tc<256, EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st)
+                          : launch_tc<128, EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st);
   }
-  r = (s->act == MOE_SWIGLU) ? launch_simt<EPI_SWIGLU>(s, x_perm, d, w_gate, w_up, F, offsets, h, F, st)
-                             : launch_simt<EPI_GELU>(s, x_perm, d, w_gate, nullptr, F, offsets, h, F, st);
+  if (src.perm != nullptr) return MOE_ERR_UNSUPPORTED;    // fp32: the rows are always permuted first
+  r = (s->act == MOE_SWIGLU) ? launch_simt<EPI_SWIGLU>(s, src.a, d, w_gate, w_up, F, offsets, h, F, st)
+                             : launch_simt<EPI_GELU>(s, src.a, d, w_gate, nullptr, F, offsets, h, F, st);
   if (r != MOE_OK) return r;
   return launch_simt<EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
 }
@@ -563,9 +592,13 @@ moe_status forward_impl(const moe_shape* s, const void* x, const float* wg, cons
   int32_t* cnt = counts ? counts : b.counts;
   moe_status r = route_impl(s, x, wg, bias, idx, w, st, o.bias_select, o.load_stats, b.stats_ws);
   if (r != MOE_OK) return r;
+  // the grouping writes the permuted copy x_perm, which the first grouped GEMM
+  // reads in whole tiles: measured faster than gathering the rows of x in the
+  // GEMM (moe_grouped_ffn_gather), whose per-row loads slow the weight stream
   r = permute_impl(s, idx, x, cnt, b.offsets, b.perm, b.inv_perm, b.x_perm, b.perm_ws, st, o.capacity, o.dropped);
   if (r != MOE_OK) return r;
-  r = ffn_impl(s, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st, o.tiling);
+  r = ffn_impl(s, RowSource{b.x_perm, nullptr, 0}, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st,
+               o.tiling);
   if (r != MOE_OK) return r;
   return combine_impl(s, b.y_perm, b.inv_perm, w, out, st);
 }
@@ -650,7 +683,7 @@ moe_status ec_forward_impl(const moe_shape* s, int64_t C, const void* x, const f
   const moe_shape f = ec_ffn_shape(s, C);
   r = launch_row_copy(s, b.inv, x, s->N, f.T, b.x_perm, st);
   if (r != MOE_OK) return r;
-  r = ffn_impl(&f, b.x_perm, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st);
+  r = ffn_impl(&f, RowSource{b.x_perm, nullptr, 0}, b.offsets, w_gate, w_up, w_down, b.y_perm, b.ffn_ws, st);
   if (r != MOE_OK) return r;
   return combine_impl(&slots, b.y_perm, b.inv, b.w, out, st);
 }
@@ -743,8 +776,10 @@ moe_status moe_permute(const moe_shape* s, const int32_t* topk_idx, const void* 
   moe_status st = shape_status(s);
   if (st != MOE_OK) return st;
   const bool any = s->T > 0;
-  if (!ptr_ok(topk_idx, any) || !ptr_ok(x, any) || !ptr_ok(counts, true) || !ptr_ok(offsets, true) ||
-      !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, any) || !ptr_ok(ws, permute_ws(s) > 0))
+  // x_perm may be NULL: the indices only (the grouped GEMM can gather the rows itself)
+  if (!ptr_ok(topk_idx, any) || !ptr_ok(x, any && x_perm != nullptr) || !ptr_ok(counts, true) ||
+      !ptr_ok(offsets, true) || !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, false) ||
+      !ptr_ok(ws, permute_ws(s) > 0))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < permute_ws(s)) return MOE_ERR_WORKSPACE;
   return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, static_cast<cudaStream_t>(stream));
@@ -757,9 +792,10 @@ moe_status moe_permute_capacity(const moe_shape* s, const int32_t* topk_idx, con
   if (st != MOE_OK) return st;
   if (!(capacity_factor >= 0.0)) return MOE_ERR_INVALID_ARG;
   const bool any = s->T > 0;
-  if (!ptr_ok(topk_idx, any) || !ptr_ok(x, any) || !ptr_ok(counts, true) || !ptr_ok(offsets, true) ||
-      !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, any) || !ptr_ok(dropped, false) ||
-      !ptr_ok(ws, permute_ws(s) > 0))
+  // x_perm may be NULL: the indices only (as moe_permute)
+  if (!ptr_ok(topk_idx, any) || !ptr_ok(x, any && x_perm != nullptr) || !ptr_ok(counts, true) ||
+      !ptr_ok(offsets, true) || !ptr_ok(perm, any) || !ptr_ok(inv_perm, any) || !ptr_ok(x_perm, false) ||
+      !ptr_ok(dropped, false) || !ptr_ok(ws, permute_ws(s) > 0))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < permute_ws(s)) return MOE_ERR_WORKSPACE;
   return permute_impl(s, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, static_cast<cudaStream_t>(stream),
@@ -776,7 +812,23 @@ moe_status moe_grouped_ffn(const moe_shape* s, const void* x_perm, const int32_t
       !ptr_ok(y_perm, any) || !ptr_ok(ws, ffn_ws(s) > 0))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < ffn_ws(s)) return MOE_ERR_WORKSPACE;
-  return ffn_impl(s, x_perm, offsets, w_gate, w_up, w_down, y_perm, ws, static_cast<cudaStream_t>(stream));
+  return ffn_impl(s, RowSource{x_perm, nullptr, 0}, offsets, w_gate, w_up, w_down, y_perm, ws,
+                  static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_grouped_ffn_gather(const moe_shape* s, const void* x, const int32_t* perm, const int32_t* offsets,
+                                  const void* w_gate, const void* w_up, const void* w_down, void* y_perm, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  moe_status st = shape_status(s);
+  if (st != MOE_OK) return st;
+  if (s->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  const bool any = s->T > 0;
+  if (!ptr_ok(x, any) || !ptr_ok(perm, any) || !ptr_ok(offsets, true) || !weights_ok(s, w_gate, w_up, w_down) ||
+      !ptr_ok(y_perm, any) || !ptr_ok(ws, ffn_ws(s) > 0))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ffn_ws(s)) return MOE_ERR_WORKSPACE;
+  return ffn_impl(s, RowSource{x, perm, s->T}, offsets, w_gate, w_up, w_down, y_perm, ws,
+                  static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_combine(const moe_shape* s, const void* y_perm, const int32_t* inv_perm, const float* topk_w,

@@ -179,3 +179,41 @@ def test_tilings_agree_within_tolerance():
         assert rel_err(got, ref) <= tol("bf16"), mode
     assert rel_err(outs["rows"], outs["tokens"]) <= tol("bf16")
     assert rel_err(outs["pairs"], outs["tokens"]) <= tol("bf16")
+
+
+@pytest.mark.parametrize("T,N,k,d,F,act", [(300, 8, 2, 256, 384, "swiglu"), (1000, 16, 4, 512, 256, "gelu_tanh"),
+                                           (37, 64, 8, 256, 192, "swiglu"), (2000, 4, 2, 4096, 512, "gelu_tanh")])
+def test_gathered_rows_equal_the_permuted_copy(T, N, k, d, F, act, tiling):
+    """moe_grouped_ffn_gather (token rows loaded through perm by the GEMM's TMA
+    gathers) gives the same bits as moe_grouped_ffn on the x_perm copy, and
+    moe_permute without x_perm gives the same indices."""
+    g = torch.Generator().manual_seed(T + N)
+    idx = torch.stack([torch.randperm(N, generator=g)[:k] for _ in range(T)]).to(torch.int32).cuda()
+    w = S.Workload("gather", T=T, d=d, N=N, k=k, F=F, act=act, dtype="bf16", seed=T)
+    x = dev(S.x_all(w))
+    ex = [S.expert_weights(w, e) for e in range(N)]
+    WG, WD = dev(np.stack([e[0] for e in ex])), dev(np.stack([e[2] for e in ex]))
+    WU = dev(np.stack([e[1] for e in ex])) if act == "swiglu" else None
+    s = B.shape(T, d, N, k, F, act, "bf16")
+    A = T * k
+    bufs = lambda: (new((N,), "i32"), new((N + 1,), "i32"), new((A,), "i32"), new((A,), "i32"))
+    ref_idx, got_idx = bufs(), bufs()
+    xp = new((A, d), "bf16")
+    ws = B.workspace(max(B.permute_workspace_size(s), B.grouped_ffn_workspace_size(s)))
+    B.permute(s, idx, x, *ref_idx, xp, ws)
+    B.permute(s, idx, x, *got_idx, None, ws)
+    for a, b in zip(ref_idx, got_idx):
+        assert torch.equal(a, b)
+    y_ref, y_got = new((A, d), "bf16", fill=0), new((A, d), "bf16", fill=0)
+    B.grouped_ffn(s, xp, ref_idx[1], WG, WU, WD, y_ref, ws)
+    B.grouped_ffn_gather(s, x, got_idx[2], got_idx[1], WG, WU, WD, y_got, ws)
+    assert B.get_error() == B.MOE_OK
+    assert torch.equal(y_ref, y_got)
+
+
+def test_gather_rejects_fp32():
+    s = B.shape(4, 128, 2, 1, 64, "swiglu", "f32")
+    z = torch.zeros(16, dtype=torch.float32, device="cuda")
+    with pytest.raises(B.MoEError) as e:
+        B.grouped_ffn_gather(s, z, z, z, z, z, z, z, B.workspace(1 << 20))
+    assert e.value.status == B.MOE_ERR_UNSUPPORTED

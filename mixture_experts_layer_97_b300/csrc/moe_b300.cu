@@ -298,6 +298,15 @@ moe_status permute_impl(const moe_shape* s, const int32_t* idx, const void* x, i
                         int32_t* perm, int32_t* inv_perm, void* x_perm, void* ws, cudaStream_t st,
                         long long capacity = kNoCapacity, int32_t* dropped = nullptr) {
   const int64_t C = perm_chunks(s);
+  if (C == 1) {   // one chunk of whole tokens (T*k <= 2048): grouping and row copy in one launch
+    const int64_t nv = static_cast<int64_t>(s->d) * esize(s) / 16;
+    const int64_t copy_warps = x_perm != nullptr ? s->T * copy_groups(nv) : 0;
+    const int64_t grid = copy_warps > 0 ? (copy_warps + kPermWarps - 1) / kPermWarps : 1;
+    permute_single_kernel<<<static_cast<unsigned>(grid), kPermThreads, 0, st>>>(
+        idx, s->T, s->N, s->k, capacity, counts, offsets, perm, inv_perm, dropped, static_cast<const uint4*>(x), nv,
+        static_cast<uint4*>(x_perm));
+    return launched();
+  }
   int32_t* hist = static_cast<int32_t*>(ws);
   if (C > 0) {
     permute_hist_kernel<<<static_cast<unsigned>(C), kPermThreads, 0, st>>>(idx, s->T, s->N, s->k, hist);

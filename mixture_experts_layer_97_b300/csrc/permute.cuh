@@ -5,8 +5,9 @@
 // count per expert, exclusive prefix sum into offsets, then move every
 // assignment's input row into one contiguous buffer ordered by expert.
 //
-// A deterministic stable counting sort by flat index f = t*k + j, in four
-// launches:
+// A deterministic stable counting sort by flat index f = t*k + j. A batch of
+// at most one chunk (T*k <= 2048, e.g. decode) takes one launch
+// (permute_single_kernel); otherwise four:
 //   hist    per chunk of whole tokens (at most 2048 assignments): expert
 //           histogram (shared-memory integer atomics: counts do not depend
 //           on their order)
@@ -181,6 +182,146 @@ constexpr int kCopyUnroll = 4;
 
 __host__ __device__ inline int64_t copy_groups(int64_t nv) { return (nv + 32 * kCopyUnroll - 1) / (32 * kCopyUnroll); }
 
+// One warp's share of the row copy: token t, chunk group gi; row_of(j) gives
+// the permuted row of assignment (t, j) (negative or >= A: not copied).
+template <typename RowOf>
+__device__ __forceinline__ void copy_token_slice(const uint4* __restrict__ x, uint4* __restrict__ x_perm, int64_t t,
+                                                 int64_t gi, int k, int64_t A, int64_t nv, int lane, RowOf row_of) {
+  const int64_t v0 = gi * 32 * kCopyUnroll + lane;
+  uint4 val[kCopyUnroll];
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u)
+    if (v0 + 32 * u < nv) val[u] = x[t * nv + v0 + 32 * u];
+  for (int j = 0; j < k; ++j) {
+    const int64_t row = row_of(j);
+    if (row < 0 || row >= A) continue;
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (v0 + 32 * u < nv) x_perm[row * nv + v0 + 32 * u] = val[u];
+  }
+}
+
+// A grouping that fits one chunk (T*k <= 2048 assignments, e.g. a decode
+// batch) in one launch instead of four: every CTA computes the per-warp
+// histograms of the rank pass, the counts / capacity / offsets of the scan
+// pass and the stable ranks (a few thousand assignments at most, so the
+// repeated work is cheaper than more launches); CTA 0 writes counts, offsets,
+// perm, inv_perm and *dropped, and all CTAs share the row copy (x_perm ==
+// nullptr: no copy, one CTA). Same results bit for bit as hist + scan + rank
+// + copy; an expert index outside [0, N) records MOE_ERR_CORRUPT (the
+// assignment belongs to no expert).
+__global__ void __launch_bounds__(kPermThreads) permute_single_kernel(const int32_t* __restrict__ topk_idx, int64_t T,
+                                                                      int N, int k, long long capacity,
+                                                                      int32_t* __restrict__ counts,
+                                                                      int32_t* __restrict__ offsets,
+                                                                      int32_t* __restrict__ perm,
+                                                                      int32_t* __restrict__ inv_perm,
+                                                                      int32_t* __restrict__ dropped,
+                                                                      const uint4* __restrict__ x, int64_t nv,
+                                                                      uint4* __restrict__ x_perm) {
+  __shared__ int wh[kPermWarps][256];
+  __shared__ int s_off[256];
+  __shared__ int s_row[kPermMaxChunk];
+  __shared__ int warp_sums[kPermWarps];
+  const bool writer = blockIdx.x == 0;
+  const int nf = static_cast<int>(T * k);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int i = threadIdx.x; i < kPermWarps * 256; i += blockDim.x) (&wh[0][0])[i] = 0;
+  __syncthreads();
+  const int s0 = warp * kPermSub;
+  const int s1 = min(nf, s0 + kPermSub);
+  // per-warp histograms over contiguous sub-ranges
+  for (int g = s0; g < s1; g += 32) {
+    const int fl = g + lane;
+    int e = (fl < s1) ? topk_idx[fl] : -1;
+    if (fl < s1 && (e < 0 || e >= N)) {
+      if (writer) record_error(MOE_ERR_CORRUPT);
+      e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // per expert: prefix over warps, the kept count, then the exclusive scan over experts
+  const int n = threadIdx.x;
+  int run = 0;
+  if (n < N) {
+#pragma unroll
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int v = wh[w][n];
+      wh[w][n] = run;
+      run += v;
+    }
+  }
+  const int kept = n < N ? static_cast<int>(run < capacity ? run : capacity) : 0;
+  int incl = kept;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int i = 0; i < warp; ++i) wbase += warp_sums[i];
+  if (n < N) {
+    s_off[n] = wbase + incl - kept;
+    if (writer) {
+      counts[n] = kept;
+      offsets[n] = wbase + incl - kept;
+    }
+  }
+  if (writer && n == kPermThreads - 1) offsets[N] = wbase + incl;
+  __syncthreads();
+  // stable ranks in flat order; rank >= capacity is dropped
+  int n_drop = 0;
+  for (int g = s0; g < s1; g += 32) {
+    const int fl = g + lane;
+    int e = (fl < s1) ? topk_idx[fl] : -1;
+    if (e >= N) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int rank = -1;
+    if (e >= 0) rank = wh[warp][e] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
+    __syncwarp();
+    if (fl < s1) {
+      int row = -1;
+      if (e >= 0) {
+        if (rank < capacity) {
+          row = s_off[e] + rank;
+          if (writer) perm[row] = fl / k;
+        } else {
+          row = kDroppedRow;
+          ++n_drop;
+        }
+      }
+      s_row[fl] = row;
+      if (writer) inv_perm[fl] = row;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) n_drop += __shfl_xor_sync(0xffffffffu, n_drop, off);
+  __syncthreads();                         // s_row complete; warp_sums free again
+  if (lane == 0) warp_sums[warp] = n_drop;
+  __syncthreads();
+  if (writer && dropped != nullptr && threadIdx.x == 0) {
+    int tot = 0;
+    for (int w = 0; w < kPermWarps; ++w) tot += warp_sums[w];
+    *dropped = tot;
+  }
+  if (x_perm == nullptr) return;
+  // the row copy, shared by all CTAs: warp gw owns (token gw / G, chunk group gw % G)
+  const int64_t G = copy_groups(nv);
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kPermWarps;
+  for (int64_t gw = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp; gw < T * G; gw += nw) {
+    const int64_t t = gw / G;
+    copy_token_slice(x, x_perm, t, gw % G, k, nf, nv, lane, [&](int j) { return s_row[t * k + j]; });
+  }
+}
+
 __global__ void __launch_bounds__(256) permute_copy_kernel(const int32_t* __restrict__ inv_perm,
                                                            const uint4* __restrict__ x, int64_t T, int k,
                                                            int64_t A, int64_t nv, uint4* __restrict__ x_perm) {
@@ -189,18 +330,7 @@ __global__ void __launch_bounds__(256) permute_copy_kernel(const int32_t* __rest
   const int lane = threadIdx.x & 31;
   if (gw >= T * G) return;
   const int64_t t = gw / G;
-  const int64_t v0 = (gw % G) * 32 * kCopyUnroll + lane;
-  uint4 val[kCopyUnroll];
-#pragma unroll
-  for (int u = 0; u < kCopyUnroll; ++u)
-    if (v0 + 32 * u < nv) val[u] = x[t * nv + v0 + 32 * u];
-  for (int j = 0; j < k; ++j) {
-    const int64_t row = inv_perm[t * k + j];
-    if (row < 0 || row >= A) continue;
-#pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u)
-      if (v0 + 32 * u < nv) x_perm[row * nv + v0 + 32 * u] = val[u];
-  }
+  copy_token_slice(x, x_perm, t, gw % G, k, A, nv, lane, [&](int j) { return static_cast<int64_t>(inv_perm[t * k + j]); });
 }
 
 }  // namespace moe

@@ -63,6 +63,9 @@ def xs(T, d, dtype, seed=0):
     (515, 256, 4, 128, "bf16"),
     (64, 8, 2, 128, "f32"),
     (50, 9, 9, 12, "f32"),           # k = N
+    (256, 64, 8, 3584, "bf16"),      # exactly one chunk (2048 assignments): the one-launch grouping
+    (1024, 16, 2, 128, "bf16"),      # one chunk
+    (1025, 16, 2, 128, "bf16"),      # one token more: two chunks
 ])
 def test_permute_random(T, N, k, d, dtype):
     compare(random_idx(T, N, k, T * 7 + N), xs(T, d, dtype, T), N, dtype)
@@ -92,8 +95,9 @@ def test_permute_empty_input():
     assert c.tolist() == [0] * 8 and o.tolist() == [0] * 9
 
 
-def test_permute_corrupt_index_recorded():
-    idx = random_idx(300, 8, 2, 1)
+@pytest.mark.parametrize("T", [300, 3000])     # one chunk (one launch) and several chunks
+def test_permute_corrupt_index_recorded(T):
+    idx = random_idx(T, 8, 2, 1)
     idx[17, 1] = 8                     # out of range
     T, k = idx.shape
     s = B.shape(T, 128, 8, k, 64, "swiglu", "bf16")

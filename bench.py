@@ -408,7 +408,10 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
     # Each stage captured once as a CUDA graph (the library only queues work on the caller's stream)
     # and replayed between event pairs: a stage's own launches (four for the grouping) run without
     # host gaps, and the events still give the per-stage breakdown.
-    graphs = None
+    # The whole step captured once as a CUDA graph (the library only queues work on the caller's
+    # stream) and replayed between two events: the step's timing. Each stage also captured on its
+    # own and replayed between event pairs in separate steps: the per-stage breakdown.
+    graphs = whole = None
     try:
         graphs = []
         cap = torch.cuda.Stream()
@@ -419,22 +422,37 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
                 with torch.cuda.graph(g, stream=cap):
                     fn()
             graphs.append(g)
+        whole = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(whole, stream=cap):
+                for fn in stages:
+                    fn()
         torch.cuda.synchronize()
         for g in graphs:
             g.replay()
+        whole.replay()
         torch.cuda.synchronize()
         stages = [g.replay for g in graphs]
     except RuntimeError:
-        graphs = None
+        graphs = whole = None
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
+        # whole-step and staged steps alternate, so both see the same power and clock state
         for i in range(steps):
             flush_l2()                         # L2 flush between timed steps (outside the events)
+            wev[i][0].record(stream)
+            if whole is not None:
+                whole.replay()
+            else:
+                step()
+            wev[i][1].record(stream)
+            flush_l2()
             step(evs[i])
         torch.cuda.synchronize()
         clk.mark_end()
@@ -444,7 +462,8 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
     if st != B.MOE_OK:
         raise RuntimeError(f"device error during timing: {B.status_string(st)}")
     stage = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
-    per_step = np.array([e[0].elapsed_time(e[4]) for e in evs])
+    per_step = np.array([a.elapsed_time(b) for a, b in wev])
+    staged_ms = float(np.median([e[0].elapsed_time(e[4]) for e in evs]))
     ffn_ms = float(np.median(stage[:, 2]))
     step_ms = max_over_ranks(float(np.median(per_step)), dist, "cuda")
 
@@ -587,6 +606,7 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
                           f"whose experts lie in a {len(cpu_used)}-expert subset; {secs:.1f} s")}
     stage_ms = {"route": float(np.median(stage[:, 0])), "permute": float(np.median(stage[:, 1])),
                 "grouped_ffn": ffn_ms, "combine": float(np.median(stage[:, 3]))}
+    stage_ms["staged_sum_of_stages"] = staged_ms
     return dict(w=w, C=C, ec=ec, cf=cf, gather=gather, step_ms=step_ms, ffn_ms=ffn_ms, stage_ms=stage_ms, cnt=cnt,
                 ffn_flops=ffn_flops, roof=roof, cpu=cpu, e2e=e2e, clocks=clk.summary(),
                 routing_stats=routing_stats, dropped=int(dropped.item()) if cf is not None else 0,
@@ -692,7 +712,10 @@ def main():
                    "token_rows": "gathered by the grouped GEMM through perm" if r["gather"] else "x_perm copy",
                    "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write, then 2 x 126 MB read of another buffer); expert weights also exceed L2"},
-        "timing": ("median over steps; every stage is a CUDA-graph replay between CUDA events on the stream"
+        "timing": ("median over steps of one CUDA-graph replay of the whole step between two CUDA events on "
+                   "the stream; stage_ms: median over steps alternating with those, in which each stage is its own "
+                   "graph replay between event pairs (their sum, staged_sum_of_stages, adds the gaps between "
+                   "replays)"
                    if r["graphs"] else "median over steps of eager stage calls between CUDA events"),
         "ffn_tflops": r["ffn_flops"] / (r["ffn_ms"] * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (r["step_ms"] * 1e-3) / 1e12,
@@ -701,9 +724,11 @@ def main():
         "routing_stats": r["routing_stats"], "dropped_assignments": r["dropped"],
         "roofline": r["roof"], "route_roofline": route_roofline(r, fma), "fma_peak": fma,
         "cpu_baseline": r["cpu"], "e2e": r["e2e"],
-        # token choice: route 1 + grouping 3 (hist, scan, rank) + row copy 1 unless gathered + grouped FFN 2
-        # + combine 1; expert choice: route 1 + select 1 + row copy 1 + grouped FFN 2 + combine 1
-        "gpu_launches": (6 if ec else (7 if r["gather"] else 8)) * args.steps,
+        # per step: token choice: route 1 + grouping (1 launch for T*k <= 2048, else hist, scan, rank and the
+        # row copy unless gathered) + grouped FFN 2 + combine 1; expert choice: route 1 + select 1 + row copy 1
+        # + grouped FFN 2 + combine 1; the timed region runs 2 x steps steps (whole-step graph, then staged)
+        "gpu_launches": 2 * args.steps * (6 if ec else (1 + (1 if w.T * w.k <= 2048 else (3 if r["gather"] else 4))
+                                                        + 2 + 1)),
         "clocks": r["clocks"],
         "decode": dec,
         "kernel_source": kernel_source_hash(),

@@ -221,24 +221,39 @@ __global__ void __launch_bounds__(kPermThreads) permute_single_kernel(const int3
                                                                       uint4* __restrict__ x_perm) {
   __shared__ int wh[kPermWarps][256];
   __shared__ int s_off[256];
-  __shared__ int s_row[kPermMaxChunk];
+  __shared__ int s_idx[kPermMaxChunk];     // the expert indices, then the permuted row of each assignment
   __shared__ int warp_sums[kPermWarps];
   const bool writer = blockIdx.x == 0;
   const int nf = static_cast<int>(T * k);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
+  // this CTA's first share of the row copy is loaded now: its latency overlaps the ranking below
+  const int64_t G = copy_groups(nv);
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kPermWarps;
+  const int64_t gw0 = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp;
+  uint4 first[kCopyUnroll];
+  if (x_perm != nullptr && gw0 < T * G) {
+    const int64_t v0 = (gw0 % G) * 32 * kCopyUnroll + lane;
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (v0 + 32 * u < nv) first[u] = x[(gw0 / G) * nv + v0 + 32 * u];
+  }
   for (int i = threadIdx.x; i < kPermWarps * 256; i += blockDim.x) (&wh[0][0])[i] = 0;
+  for (int f = threadIdx.x; f < nf; f += blockDim.x) {
+    int e = topk_idx[f];
+    if (e < 0 || e >= N) {
+      if (writer) record_error(MOE_ERR_CORRUPT);
+      e = -1;                              // belongs to no expert
+    }
+    s_idx[f] = e;
+  }
   __syncthreads();
   const int s0 = warp * kPermSub;
   const int s1 = min(nf, s0 + kPermSub);
   // per-warp histograms over contiguous sub-ranges
   for (int g = s0; g < s1; g += 32) {
     const int fl = g + lane;
-    int e = (fl < s1) ? topk_idx[fl] : -1;
-    if (fl < s1 && (e < 0 || e >= N)) {
-      if (writer) record_error(MOE_ERR_CORRUPT);
-      e = -1;
-    }
+    const int e = (fl < s1) ? s_idx[fl] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && (peers & lt_mask) == 0) wh[warp][e] += __popc(peers);
     __syncwarp();
@@ -275,12 +290,12 @@ __global__ void __launch_bounds__(kPermThreads) permute_single_kernel(const int3
   }
   if (writer && n == kPermThreads - 1) offsets[N] = wbase + incl;
   __syncthreads();
-  // stable ranks in flat order; rank >= capacity is dropped
+  // stable ranks in flat order (each warp its own sub-range, so s_idx can take the rows in place);
+  // rank >= capacity is dropped
   int n_drop = 0;
   for (int g = s0; g < s1; g += 32) {
     const int fl = g + lane;
-    int e = (fl < s1) ? topk_idx[fl] : -1;
-    if (e >= N) e = -1;
+    const int e = (fl < s1) ? s_idx[fl] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     int rank = -1;
     if (e >= 0) rank = wh[warp][e] + __popc(peers & lt_mask);
@@ -298,13 +313,13 @@ __global__ void __launch_bounds__(kPermThreads) permute_single_kernel(const int3
           ++n_drop;
         }
       }
-      s_row[fl] = row;
+      s_idx[fl] = row;
       if (writer) inv_perm[fl] = row;
     }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) n_drop += __shfl_xor_sync(0xffffffffu, n_drop, off);
-  __syncthreads();                         // s_row complete; warp_sums free again
+  __syncthreads();                         // every row known; warp_sums free again
   if (lane == 0) warp_sums[warp] = n_drop;
   __syncthreads();
   if (writer && dropped != nullptr && threadIdx.x == 0) {
@@ -314,11 +329,20 @@ __global__ void __launch_bounds__(kPermThreads) permute_single_kernel(const int3
   }
   if (x_perm == nullptr) return;
   // the row copy, shared by all CTAs: warp gw owns (token gw / G, chunk group gw % G)
-  const int64_t G = copy_groups(nv);
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * kPermWarps;
-  for (int64_t gw = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp; gw < T * G; gw += nw) {
+  for (int64_t gw = gw0; gw < T * G; gw += nw) {
     const int64_t t = gw / G;
-    copy_token_slice(x, x_perm, t, gw % G, k, nf, nv, lane, [&](int j) { return s_row[t * k + j]; });
+    const int64_t v0 = (gw % G) * 32 * kCopyUnroll + lane;
+    uint4 val[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (v0 + 32 * u < nv) val[u] = gw == gw0 ? first[u] : x[t * nv + v0 + 32 * u];
+    for (int j = 0; j < k; ++j) {
+      const int row = s_idx[t * k + j];
+      if (row < 0 || row >= nf) continue;
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u)
+        if (v0 + 32 * u < nv) x_perm[row * nv + v0 + 32 * u] = val[u];
+    }
   }
 }
 

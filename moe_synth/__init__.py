@@ -76,6 +76,15 @@ WORKLOADS = {
     # 4096 -> 16384 -> 4096 GELU) with 8 of its 64 experts, 2.1 GB of weights
     "worked-example-slice-n8": Workload("worked-example-slice-n8", T=1024, d=4096, N=8, k=2, F=16384,
                                         act="gelu_tanh", dtype="bf16", seed=6),
+    # profiling case of the grouping and the combine: the worked example's tokens, gate and routing
+    # (same seed, T, d, N, k) with 128-wide experts, so x_perm / y_perm (134 MB) exceed L2 while the
+    # weights take 0.2 GB
+    "worked-example-f128": Workload("worked-example-f128", T=8192, d=4096, N=64, k=2, F=128,
+                                    act="gelu_tanh", dtype="bf16", seed=3),
+    # profiling case of the decode-shaped grouped GEMM: the decode batch's shapes with 16 experts
+    # (0.88 GB of weights instead of 3.5 GB)
+    "decode-slice-n16": Workload("decode-slice-n16", T=32, d=3584, N=16, k=8, F=2560, act="swiglu",
+                                 dtype="bf16", seed=4),
 }
 
 

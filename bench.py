@@ -443,7 +443,7 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         clk.mark_start()
-        # whole-step and staged steps alternate, so both see the same power and clock state
+        # the timed steps: whole-step graph replays, back to back
         for i in range(steps):
             flush_l2()                         # L2 flush between timed steps (outside the events)
             wev[i][0].record(stream)
@@ -452,10 +452,15 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
             else:
                 step()
             wev[i][1].record(stream)
-            flush_l2()
-            step(evs[i])
         torch.cuda.synchronize()
         clk.mark_end()
+    # the per-stage breakdown: as many staged steps, after a pause that lets the power state of the
+    # timed steps settle (under a sustained load the part lowers its clocks at the power cap)
+    time.sleep(0.5)
+    for i in range(steps):
+        flush_l2()
+        step(evs[i])
+    torch.cuda.synchronize()
     if dist:
         dist.barrier()
     st = B.get_error()
@@ -712,10 +717,10 @@ def main():
                    "token_rows": "gathered by the grouped GEMM through perm" if r["gather"] else "x_perm copy",
                    "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write, then 2 x 126 MB read of another buffer); expert weights also exceed L2"},
-        "timing": ("median over steps of one CUDA-graph replay of the whole step between two CUDA events on "
-                   "the stream; stage_ms: median over steps alternating with those, in which each stage is its own "
-                   "graph replay between event pairs (their sum, staged_sum_of_stages, adds the gaps between "
-                   "replays)"
+        "timing": ("median over the timed steps, each one CUDA-graph replay of the whole step between two CUDA "
+                   "events on the stream; stage_ms: median over as many later steps (after a 0.5 s pause) in "
+                   "which each stage is its own graph replay between event pairs (their sum, "
+                   "staged_sum_of_stages, adds the gaps between replays)"
                    if r["graphs"] else "median over steps of eager stage calls between CUDA events"),
         "ffn_tflops": r["ffn_flops"] / (r["ffn_ms"] * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (r["step_ms"] * 1e-3) / 1e12,
@@ -726,8 +731,8 @@ def main():
         "cpu_baseline": r["cpu"], "e2e": r["e2e"],
         # per step: token choice: route 1 + grouping (1 launch for T*k <= 2048, else hist, scan, rank and the
         # row copy unless gathered) + grouped FFN 2 + combine 1; expert choice: route 1 + select 1 + row copy 1
-        # + grouped FFN 2 + combine 1; the timed region runs 2 x steps steps (whole-step graph, then staged)
-        "gpu_launches": 2 * args.steps * (6 if ec else (1 + (1 if w.T * w.k <= 2048 else (3 if r["gather"] else 4))
+        # + grouped FFN 2 + combine 1 (the tile-counter memsets of the SM-pair GEMM are not kernels)
+        "gpu_launches": args.steps * (6 if ec else (1 + (1 if w.T * w.k <= 2048 else (3 if r["gather"] else 4))
                                                         + 2 + 1)),
         "clocks": r["clocks"],
         "decode": dec,

@@ -60,15 +60,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with acquire at cluster scope: for data another CTA of the cluster
+// wrote before a release-arrive on this barrier.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the barrier phase of the given parity has completed. Gives up
 // when *abort is set by another role, or after timeout_ns of wall time (then
 // sets *abort and records MOE_ERR_TIMEOUT). Returns false when it gave up.
+// CLUSTER: acquire at cluster scope (mbar_try_wait_cluster).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto try_once = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (try_once()) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (try_once()) return true;
     if ((it & 31u) == 0) {
       if (abort != nullptr && *abort) return false;
       if (global_ns() - t0 > timeout_ns) {
@@ -91,6 +108,11 @@ __device__ __forceinline__ uint32_t cluster_cta_rank() {
 // wait for the other CTAs'.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32-bit store to a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Address of the same shared-memory variable in CTA `rank` of the cluster.

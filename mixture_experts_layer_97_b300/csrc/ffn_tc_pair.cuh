@@ -23,6 +23,17 @@
 // the unpermuted tokens x through the permutation (perm[row] = token): lanes
 // of warp 0 gather four rows each per stage (TMA tile::gather4).
 //
+// Tiles are handed out dynamically: the even CTA's producer takes the next
+// tile id from a global counter (zeroed before the launch) whenever it starts
+// a tile, and passes it through a small queue (kPrQueue slots on mbarriers)
+// to its own MMA issuer and epilogue warps and, through distributed shared
+// memory, to the odd CTA's producer and epilogue warps; id -1 ends the loop.
+// Tile ids keep the (expert, feature tile, token tile) order, so the token
+// tiles of one weight tile still run at the same time on neighbouring pairs,
+// while tiles of unequal size no longer pile up on some pairs (on the worked
+// example's routing a static round robin gives the busiest pair 23 % more
+// work than the average in the down projection).
+//
 // Roles (both CTAs): warp 0 TMA producer for the CTA's own shared memory,
 // warp 1 TMEM (allocated by both CTAs together) and, in the even CTA only,
 // the MMA issuer; warps 2-9 epilogue on the CTA's own TMEM (its 128 weight
@@ -45,9 +56,12 @@ constexpr int kPrABytes = 2 * kPrWBytes;                    // the CTA's pair of
 constexpr int kPrBRows = kSwMaxNT / 2;                      // token rows per CTA (max)
 constexpr int kPrBBytes = kPrBRows * kPrRowBytes;           // 16 KB
 constexpr int kPrStageBytes = kPrABytes + kPrBBytes;        // 48 KB
-constexpr int kPrNumBars = 2 * kPrStages + 3;
+constexpr int kPrQueue = 4;                                 // tile ids in flight between the roles
+constexpr int kPrNumBars = 2 * kPrStages + 3 + 2 * kPrQueue;
+// consumers of a queue slot: the MMA issuer, the odd CTA's producer, 8 epilogue warps per CTA
+constexpr int kPrQueueConsumers = 2 + 2 * kSwEpiWarps;
 constexpr size_t kPrSmemBytes = 1024 + static_cast<size_t>(kPrStages) * kPrStageBytes + kSwXposeBytes +
-                                8 * kPrNumBars + 16 + 2 * 257 * sizeof(int) + 16;
+                                8 * kPrNumBars + 16 + 2 * 257 * sizeof(int) + kPrQueue * sizeof(int) + 16;
 static_assert(kPrSmemBytes <= 227 * 1024, "pair kernel shared memory");
 
 // Output features of one pair tile and of each CTA's half.
@@ -109,7 +123,8 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     grouped_gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                                 const __grid_constant__ CUtensorMap tmX, const int32_t* __restrict__ offsets, int N,
                                 int rows_total, int K, int Nout, __nv_bfloat16* __restrict__ out, int ldo,
-                                unsigned long long timeout_ns, const int32_t* __restrict__ perm) {
+                                unsigned long long timeout_ns, const int32_t* __restrict__ perm,
+                                int* __restrict__ tile_counter) {
   constexpr int S = kPrStages;
   constexpr int OFP = pr_tile_features<EPI>();      // features per pair tile
   constexpr int OFC = OFP / 2;                      // features of this CTA
@@ -127,11 +142,14 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   uint64_t* tfull_bar = bars + 2 * S;
   uint64_t* tempty_bar = tfull_bar + 1;           // used in the even CTA only
   uint64_t* drain_bar = tfull_bar + 2;
+  uint64_t* tq_full = tfull_bar + 3;              // [kPrQueue], both CTAs
+  uint64_t* tq_empty = tq_full + kPrQueue;        // [kPrQueue], used in the even CTA only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kPrNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* bad_flag = reinterpret_cast<int*>(tmem_slot + 2);
   int* s_off = reinterpret_cast<int*>(tmem_slot + 4);
   int* s_pre = s_off + 257;
+  volatile int* tq = s_pre + 257;                 // [kPrQueue] tile ids
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_cta_rank();
@@ -145,6 +163,10 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     mbar_init(smem_addr(tfull_bar), 1);
     mbar_init(smem_addr(tempty_bar), 2 * kSwEpiWarps);
     mbar_init(smem_addr(drain_bar), 1);
+    for (int q = 0; q < kPrQueue; ++q) {
+      mbar_init(smem_addr(&tq_full[q]), 1);
+      mbar_init(smem_addr(&tq_empty[q]), kPrQueueConsumers);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -172,16 +194,44 @@ __global__ void __launch_bounds__(kSwThreads, 1)
   const int n_ftiles = (Nout + OFP - 1) / OFP;
   const long long total = bad ? 0 : static_cast<long long>(s_pre[N]) * n_ftiles;
   const int KB = K / kTcBK;
-  const long long pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  // the tile queue: slot q % kPrQueue; a consumer takes use q at parity (q / kPrQueue) & 1
+  auto q_slot = [](uint32_t q) { return q % kPrQueue; };
+  auto q_par = [](uint32_t q) { return (q / kPrQueue) & 1u; };
+  // Next tile id for use q, in every role's loop (lane 0 of the calling warp
+  // answers, the warp gets the id): the even CTA's producer fetches it and
+  // publishes it to both CTAs; every other role reads it from its own queue
+  // and releases the slot on the even CTA. -1: no more tiles (or gave up).
+  auto next_tile = [&](uint32_t q, bool fetcher, bool warp_wide) -> long long {
+    long long id = -1;
+    if (lane == 0) {
+      const uint32_t sl = q_slot(q);
+      if (fetcher) {
+        if (mbar_wait_bounded(smem_addr(&tq_empty[sl]), q_par(q) ^ 1u, abort_flag, timeout_ns)) {
+          const long long v = atomicAdd(tile_counter, 1);
+          id = v < total ? v : -1;
+        }
+        tq[sl] = static_cast<int>(id);
+        st_cluster_s32(smem_addr_in_cta(smem_addr(const_cast<int*>(&tq[sl])), 1), static_cast<int>(id));
+        mbar_arrive(smem_addr(&tq_full[sl]));
+        mbar_arrive_remote(smem_addr_in_cta(smem_addr(&tq_full[sl]), 1));
+      } else {
+        if (mbar_wait_bounded<true>(smem_addr(&tq_full[sl]), q_par(q), abort_flag, timeout_ns)) id = tq[sl];
+        mbar_arrive_remote(smem_addr_in_cta(smem_addr(&tq_empty[sl]), 0));
+      }
+    }
+    return warp_wide ? __shfl_sync(0xffffffffu, id, 0) : id;
+  };
 
   if (warp == 0 && (GATHER || lane == 0)) {
-    // ---------------- TMA producer (each CTA fills its own shared memory; lane 0 waits and loads
-    // the weights, and with GATHER the first lanes gather four token rows each)
+    // ---------------- TMA producer (each CTA fills its own shared memory; lane 0 takes the tile ids,
+    // waits and loads the weights, and with GATHER the first lanes gather four token rows each)
     int s = 0;
     uint32_t ph = 0;
     long long issued = 0;
     bool ok = true;
-    for (long long id = pair; id < total && ok; id += npairs) {
+    for (uint32_t qi = 0; ok; ++qi) {
+      const long long id = next_tile(qi, leader, GATHER);
+      if (id < 0) break;
       const SwTile t = sw_decode(id, s_off, s_pre, N, n_ftiles);
       const int w0row = t.e * Nout + t.fi * OFP + static_cast<int>(rank) * OFC;
       const int w1row = (EPI == EPI_SWIGLU) ? w0row : w0row + kSwFM;
@@ -237,7 +287,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       uint32_t ph = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (long long id = pair; id < total && ok; id += npairs) {
+      for (uint32_t qi = 0; ok; ++qi) {
+        const long long id = next_tile(qi, false, false);
+        if (id < 0) break;
         const SwTile t = sw_decode(id, s_off, s_pre, N, n_ftiles);
         const uint32_t idesc = IDESC0 | (static_cast<uint32_t>(t.nt >> 3) << 17);
         if (!mbar_wait_bounded(smem_addr(tempty_bar), aph ^ 1u, abort_flag, timeout_ns)) break;
@@ -276,7 +328,9 @@ __global__ void __launch_bounds__(kSwThreads, 1)
     const uint32_t xp_s = smem_addr(xp);
     const uint32_t tempty_leader = smem_addr_in_cta(smem_addr(tempty_bar), 0);
     uint32_t aph = 0;
-    for (long long id = pair; id < total; id += npairs) {
+    for (uint32_t qi = 0;; ++qi) {
+      const long long id = next_tile(qi, false, true);
+      if (id < 0) break;
       const SwTile t = sw_decode(id, s_off, s_pre, N, n_ftiles);
       if (!mbar_wait_bounded(smem_addr(tfull_bar), aph, abort_flag, timeout_ns)) break;
       tc_fence_after();

@@ -59,7 +59,9 @@ int64_t perm_chunks(const moe_shape* s) {
 }
 
 size_t permute_ws(const moe_shape* s) { return align_up(sizeof(int32_t) * perm_chunks(s) * s->N); }
-size_t ffn_ws(const moe_shape* s) { return align_up(esize(s) * static_cast<size_t>(n_assign(s)) * s->d_ff); }
+// The grouped FFN's workspace: h [A, F], then the SM-pair GEMM's tile counter.
+size_t ffn_h_bytes(const moe_shape* s) { return align_up(esize(s) * static_cast<size_t>(n_assign(s)) * s->d_ff); }
+size_t ffn_ws(const moe_shape* s) { return ffn_h_bytes(s) + kAlign; }
 // Statistics rows of one route launch: at most one per 4 tokens, 2N + 1 floats each.
 size_t route_stats_ws(const moe_shape* s) {
   return align_up(sizeof(float) * static_cast<size_t>((s->T + 3) / 4) * (2 * static_cast<size_t>(s->N) + 1));
@@ -457,9 +459,11 @@ moe_status launch_tc_swap_bk(const moe_shape* s, const RowSource& src, int K, co
 
 // The token-tile grouped GEMM on SM pairs: clusters of two CTAs sharing
 // each MMA (tcgen05 cta_group::2).
+// tile_counter: a device int the kernel hands out tiles from; zeroed here, on
+// the stream, before the launch.
 template <int EPI>
 moe_status launch_tc_pair(const moe_shape* s, const RowSource& src, int K, const void* w0, const void* w1, int Nout,
-                          const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+                          const int32_t* offsets, void* out, int ldo, cudaStream_t st, int* tile_counter) {
   constexpr int OFP = pr_tile_features<EPI>();
   const int64_t A = n_assign(s);
   CUtensorMap mx, mw0, mw1;
@@ -472,6 +476,7 @@ moe_status launch_tc_pair(const moe_shape* s, const RowSource& src, int K, const
     mw1 = mw0;
   }
   auto kern = src.perm != nullptr ? grouped_gemm_tc_pair_kernel<EPI, true> : grouped_gemm_tc_pair_kernel<EPI, false>;
+  if (cudaMemsetAsync(tile_counter, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPrSmemBytes)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -492,18 +497,18 @@ moe_status launch_tc_pair(const moe_shape* s, const RowSource& src, int K, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, kern, mw0, mw1, mx, offsets, s->N, static_cast<int>(A), K, Nout,
-                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs, src.perm) != cudaSuccess)
+                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs, src.perm, tile_counter) != cudaSuccess)
     return MOE_ERR_CUDA;
   return launched();
 }
 
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const RowSource& src, int K, const void* w0, const void* w1, int Nout,
-                          const int32_t* offsets, void* out, int ldo, cudaStream_t st, int mode) {
+                          const int32_t* offsets, void* out, int ldo, cudaStream_t st, int mode, int* tile_counter) {
   // auto and "pairs" run token tiles on SM pairs, "tokens" on single SMs
   if (mode == MOE_TILING_TOKENS)
     return launch_tc_swap_bk<EPI, kTcBK>(s, src, K, w0, w1, Nout, offsets, out, ldo, st);
-  return launch_tc_pair<EPI>(s, src, K, w0, w1, Nout, offsets, out, ldo, st);
+  return launch_tc_pair<EPI>(s, src, K, w0, w1, Nout, offsets, out, ldo, st, tile_counter);
 }
 
 // K is the reduction length of the GEMM in question (d for the first, F for
@@ -542,12 +547,13 @@ moe_status ffn_impl(const moe_shape* s, const RowSource& src, const int32_t* off
   const int mode = tiling >= 0 ? tiling : g_ffn_tiling.load(std::memory_order_relaxed);
   void* h = ws;
   const RowSource hs{h, nullptr, 0};
+  int* ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ffn_h_bytes(s));
   moe_status r;
   if (s->dtype == MOE_BF16) {
     if (use_token_tiles(s, d, mode))
       r = (s->act == MOE_SWIGLU)
-              ? launch_tc_swap<EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st, mode)
-              : launch_tc_swap<EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st, mode);
+              ? launch_tc_swap<EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st, mode, ctr)
+              : launch_tc_swap<EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st, mode, ctr);
     else if (s->act == MOE_SWIGLU)
       r = (F % 128 == 0) ? launch_tc<256, EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st)
                          : launch_tc<128, EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st);
@@ -556,7 +562,7 @@ moe_status ffn_impl(const moe_shape* s, const RowSource& src, const int32_t* off
                          : launch_tc<128, EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st);
     if (r != MOE_OK) return r;
     if (use_token_tiles(s, F, mode))
-      return launch_tc_swap<EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st, mode);
+      return launch_tc_swap<EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st, mode, ctr);
     return (d % 256 == 0) ? launch_tc<256, EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st)
                           : launch_tc<128, EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st);
   }

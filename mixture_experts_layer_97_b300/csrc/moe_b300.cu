@@ -253,7 +253,8 @@ moe_status launch_route(const moe_shape* s, const TX* x, RouteArgs& a, cudaStrea
   // Large batches: seven tokens per thread (more independent chains per thread hide more latency
   // than more warps do) in tiles that give each SM one CTA: 56 tokens x up to 64 experts, or 112
   // tokens x up to 128 experts (8192 x 64: 154 vs 168 us at 64 tokens per CTA; 16384 x 128: 227 vs
-  // 252 us; 512-thread CTAs with fewer chains per thread were slower in both)
+  // 252 us; 512-thread CTAs with fewer chains per thread were slower in both, and so were token
+  // pairs in the packed FMAs with x widened once per CTA: 164 vs 154 us, 252 vs 229 us)
   if (s->N > 8 && s->N <= 64 && (T + 55) / 56 >= sms * 9 / 10) {
     if (s->N <= 32) return launch_route_cfg<32, 1, 7, TX>(s, x, a, st);                 // 56 tokens/CTA
     return launch_route_cfg<32, 2, 7, TX>(s, x, a, st);

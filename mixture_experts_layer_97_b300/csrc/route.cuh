@@ -169,6 +169,104 @@ __device__ __forceinline__ void topk_renorm(const float* g, const float* v, bool
   }
 }
 
+// The end of a routing CTA, shared by the route kernels: the TM x NP logit
+// tile lg[token][n] (row pitch NP + 1, padded experts -inf) is complete in
+// shared memory. One warp per token runs the top-k and the renormalised
+// weights; optionally the full softmax for the statistics rows (srow: shared
+// scratch of [THR / 32][2 NP + 1] floats, written into stats_part's row of
+// this CTA) and for probs_out.
+template <int NP, int TM, int THR>
+__device__ __forceinline__ void route_select(const float* lg, float* srow, int64_t t0, int T, int N, int k,
+                                             const float* __restrict__ bias, int bias_select,
+                                             int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                             float* __restrict__ stats_part, float* __restrict__ probs_out) {
+  constexpr int NPR = NP < 32 ? 32 : NP;   // register slots per token for the argmax
+  constexpr int SLOTS = NPR / 32;
+  // top-k: one warp per token, k rounds of warp argmax (ties -> lower id)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool want_stats = stats_part != nullptr;
+  float bsel[SLOTS];          // the bias of the choosing score when it only chooses
+  float p_acc[SLOTS];         // statistics: sum over this warp's tokens of p[t,n]
+  float c_acc[SLOTS];         //             assignments to n
+  float top1_acc = 0.f;       //             sum of the top-1 probabilities
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const int n = lane + 32 * m;
+    bsel[m] = (bias != nullptr && bias_select && n < N) ? bias[n] : 0.f;
+    p_acc[m] = 0.f;
+    c_acc[m] = 0.f;
+  }
+  for (int tl = warp; tl < TM; tl += THR / 32) {
+    const int64_t t = t0 + tl;
+    if (t >= T) break;
+    float g[SLOTS];           // logits of the softmax
+    float v[SLOTS];           // choosing scores
+    bool taken[SLOTS];
+#pragma unroll
+    for (int m = 0; m < SLOTS; ++m) {
+      const int n = lane + 32 * m;
+      g[m] = (n < NP) ? lg[tl * (NP + 1) + n] : -INFINITY;
+      v[m] = (n < N) ? g[m] + bsel[m] : -INFINITY;
+      taken[m] = (n >= N);
+    }
+    if (topk_idx != nullptr)   // top-k choice and its renormalised weights
+      topk_renorm<SLOTS>(g, v, taken, k, lane, topk_idx + t * k, topk_w + t * k, c_acc);
+    if (want_stats || probs_out != nullptr) {   // full softmax over the N experts
+      float gmax = -INFINITY;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) gmax = fmaxf(gmax, g[m]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+      float e[SLOTS], z = 0.f;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) {
+        e[m] = (lane + 32 * m < N) ? expf(g[m] - gmax) : 0.f;
+        z += e[m];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      const float iz = 1.f / z;
+#pragma unroll
+      for (int m = 0; m < SLOTS; ++m) {
+        const int n = lane + 32 * m;
+        p_acc[m] += e[m] * iz;
+        if (probs_out != nullptr && n < N) probs_out[t * N + n] = e[m] * iz;
+      }
+      top1_acc += iz;         // p of the largest logit is exp(0) / z
+    }
+  }
+  if (!want_stats) return;
+  // per-warp rows -> one row per CTA: [N probability sums | N counts | top-1 sum]
+  constexpr int SW = 2 * NP + 1;
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const int n = lane + 32 * m;
+    if (n < NP) {
+      srow[warp * SW + n] = p_acc[m];
+      srow[warp * SW + NP + n] = c_acc[m];
+    }
+  }
+  if (lane == 0) srow[warp * SW + 2 * NP] = top1_acc;
+  __syncthreads();
+  float* out = stats_part + static_cast<int64_t>(blockIdx.x) * (2 * N + 1);
+  for (int n = tid; n < N; n += THR) {
+    float ps = 0.f, cs = 0.f;
+#pragma unroll
+    for (int w = 0; w < THR / 32; ++w) {
+      ps += srow[w * SW + n];
+      cs += srow[w * SW + NP + n];
+    }
+    out[n] = ps;
+    out[N + n] = cs;
+  }
+  if (tid == 0) {
+    float ts = 0.f;
+#pragma unroll
+    for (int w = 0; w < THR / 32; ++w) ts += srow[w * SW + 2 * NP];
+    out[2 * N] = ts;
+  }
+}
+
 template <int EG, int EPT, int TPT, typename TX, int THR = kRouteThreads>
 __global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, const float* __restrict__ wg,
                                                               const float* __restrict__ bias, int T, int d, int N,
@@ -179,8 +277,6 @@ __global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, co
                                                               float* __restrict__ probs_out) {
   using C = RouteCfg<EG, EPT, TPT, TX, THR>;
   constexpr int NP = C::NP, TM = C::TM, S = C::STAGES;
-  constexpr int NPR = NP < 32 ? 32 : NP;   // register slots per token for the argmax
-  constexpr int SLOTS = NPR / 32;
   constexpr int XCH = kRouteBK * static_cast<int>(sizeof(TX)) / 16;   // 16-byte chunks per token row slice
   extern __shared__ __align__(16) uint8_t route_smem[];
   uint8_t* xs = route_smem;                      // [S][TM][XROW bytes]
@@ -315,90 +411,8 @@ __global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, co
   }
   __syncthreads();
 
-  // top-k: one warp per token, k rounds of warp argmax (ties -> lower id)
-  const int warp = tid >> 5, lane = tid & 31;
-  const bool want_stats = stats_part != nullptr;
-  float bsel[SLOTS];          // the bias of the choosing score when it only chooses
-  float p_acc[SLOTS];         // statistics: sum over this warp's tokens of p[t,n]
-  float c_acc[SLOTS];         //             assignments to n
-  float top1_acc = 0.f;       //             sum of the top-1 probabilities
-#pragma unroll
-  for (int m = 0; m < SLOTS; ++m) {
-    const int n = lane + 32 * m;
-    bsel[m] = (bias != nullptr && bias_select && n < N) ? bias[n] : 0.f;
-    p_acc[m] = 0.f;
-    c_acc[m] = 0.f;
-  }
-  for (int tl = warp; tl < TM; tl += THR / 32) {
-    const int64_t t = t0 + tl;
-    if (t >= T) break;
-    float g[SLOTS];           // logits of the softmax
-    float v[SLOTS];           // choosing scores
-    bool taken[SLOTS];
-#pragma unroll
-    for (int m = 0; m < SLOTS; ++m) {
-      const int n = lane + 32 * m;
-      g[m] = (n < NP) ? lg[tl * (NP + 1) + n] : -INFINITY;
-      v[m] = (n < N) ? g[m] + bsel[m] : -INFINITY;
-      taken[m] = (n >= N);
-    }
-    if (topk_idx != nullptr)   // top-k choice and its renormalised weights
-      topk_renorm<SLOTS>(g, v, taken, k, lane, topk_idx + t * k, topk_w + t * k, c_acc);
-    if (want_stats || probs_out != nullptr) {   // full softmax over the N experts
-      float gmax = -INFINITY;
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m) gmax = fmaxf(gmax, g[m]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
-      float e[SLOTS], z = 0.f;
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m) {
-        e[m] = (lane + 32 * m < N) ? expf(g[m] - gmax) : 0.f;
-        z += e[m];
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-      const float iz = 1.f / z;
-#pragma unroll
-      for (int m = 0; m < SLOTS; ++m) {
-        const int n = lane + 32 * m;
-        p_acc[m] += e[m] * iz;
-        if (probs_out != nullptr && n < N) probs_out[t * N + n] = e[m] * iz;
-      }
-      top1_acc += iz;         // p of the largest logit is exp(0) / z
-    }
-  }
-  if (!want_stats) return;
-  // per-warp rows -> one row per CTA: [N probability sums | N counts | top-1 sum]
-  float* srow = reinterpret_cast<float*>(route_smem + C::kLogits);   // [THR / 32][2*NP + 1]
-  constexpr int SW = 2 * NP + 1;
-#pragma unroll
-  for (int m = 0; m < SLOTS; ++m) {
-    const int n = lane + 32 * m;
-    if (n < NP) {
-      srow[warp * SW + n] = p_acc[m];
-      srow[warp * SW + NP + n] = c_acc[m];
-    }
-  }
-  if (lane == 0) srow[warp * SW + 2 * NP] = top1_acc;
-  __syncthreads();
-  float* out = stats_part + static_cast<int64_t>(blockIdx.x) * (2 * N + 1);
-  for (int n = tid; n < N; n += THR) {
-    float ps = 0.f, cs = 0.f;
-#pragma unroll
-    for (int w = 0; w < THR / 32; ++w) {
-      ps += srow[w * SW + n];
-      cs += srow[w * SW + NP + n];
-    }
-    out[n] = ps;
-    out[N + n] = cs;
-  }
-  if (tid == 0) {
-    float ts = 0.f;
-#pragma unroll
-    for (int w = 0; w < THR / 32; ++w) ts += srow[w * SW + 2 * NP];
-    out[2 * N] = ts;
-  }
+  route_select<NP, TM, THR>(lg, reinterpret_cast<float*>(route_smem + C::kLogits), t0, T, N, k, bias, bias_select,
+                            topk_idx, topk_w, stats_part, probs_out);
 }
 
 // Small batches (decode): each logit chain is d sequential FMAs, so the time

@@ -85,6 +85,10 @@ WORKLOADS = {
     # (0.88 GB of weights instead of 3.5 GB)
     "decode-slice-n16": Workload("decode-slice-n16", T=32, d=3584, N=16, k=8, F=2560, act="swiglu",
                                  dtype="bf16", seed=4),
+    # profiling case of the decode batch's routing, grouping and combine: its tokens, gate and
+    # routing (same seed, T, d, N, k) with 128-wide experts (0.18 GB of weights instead of 3.5 GB)
+    "decode-f128": Workload("decode-f128", T=32, d=3584, N=64, k=8, F=128, act="swiglu", dtype="bf16",
+                            seed=4),
 }
 
 

@@ -134,11 +134,12 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Samples between t0 and t1 (monotonic; default: mark_start / mark_end)."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        t0 = self.t0 if self.t0 is not None else float("-inf")
-        t1 = self.t1 if self.t1 is not None else float("inf")
+        t0 = t0 if t0 is not None else (self.t0 if self.t0 is not None else float("-inf"))
+        t1 = t1 if t1 is not None else (self.t1 if self.t1 is not None else float("inf"))
         after = [ts for ts, _ in self.lines if ts > t1]
         t1 = min(after) if after else t1      # include the first sample after the region
         for ts, ln in self.lines:
@@ -454,13 +455,20 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
             wev[i][1].record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
-    # the per-stage breakdown: as many staged steps, after a pause that lets the power state of the
-    # timed steps settle (under a sustained load the part lowers its clocks at the power cap)
-    time.sleep(0.5)
-    for i in range(steps):
-        flush_l2()
-        step(evs[i])
-    torch.cuda.synchronize()
+        # the per-stage breakdown: as many staged steps, after a pause that lets the power state of
+        # the timed steps settle (under a sustained load the part lowers its clocks at the power cap);
+        # each staged step runs alone (synchronised, then a short idle gap), so its kernels are timed
+        # in isolation, the condition of the burst peaks they are compared with
+        time.sleep(0.5)
+        ts0 = time.monotonic()
+        for i in range(steps):
+            flush_l2()
+            step(evs[i])
+            torch.cuda.synchronize()
+            time.sleep(0.02)
+        ts1 = time.monotonic()
+        time.sleep(0.12)
+        clocks_staged = clk.summary(ts0, ts1)
     if dist:
         dist.barrier()
     st = B.get_error()
@@ -614,6 +622,7 @@ def measure(w: S.Workload, args, torch, B, world: int, rank: int, local: int, di
     stage_ms["staged_sum_of_stages"] = staged_ms
     return dict(w=w, C=C, ec=ec, cf=cf, gather=gather, step_ms=step_ms, ffn_ms=ffn_ms, stage_ms=stage_ms, cnt=cnt,
                 ffn_flops=ffn_flops, roof=roof, cpu=cpu, e2e=e2e, clocks=clk.summary(),
+                clocks_staged=clocks_staged,
                 routing_stats=routing_stats, dropped=int(dropped.item()) if cf is not None else 0,
                 graphs=graphs is not None, fwd_bytes=fwd_bytes, P=P)
 
@@ -630,6 +639,56 @@ def route_roofline(r: dict, fma: Optional[dict]) -> dict:
         out.update({"peak": fma["peak"], "frac": ach / fma["peak"],
                     "peak_kind": "measured fp32 FMA (libmoe_fma_peak.so: " + fma["how"] + ")"})
     return out
+
+
+def measure_ep_local(w: S.Workload, cnt: np.ndarray, torch, B, G: int, hbm_gbs: float, steps: int = 20) -> dict:
+    """The receiving rank's local steps of expert parallelism (moe_ep_regroup,
+    moe_ep_ungroup) at the workload's size, as if its experts were split over G
+    ranks: the count table is the workload's own per-expert counts read as G
+    sources x E = N / G local experts, so the rank receives all T*k rows. Each
+    kernel reads and writes rows x d once (algorithmic bytes 2 rows d es); the
+    all-to-all between ranks is not part of it (one GPU)."""
+    E = w.N // G
+    table = np.ascontiguousarray(cnt.reshape(G, E), dtype=np.int32)
+    rows = int(table.sum())
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    es = 2 if w.dtype == "bf16" else 4
+    rc = torch.from_numpy(table.reshape(-1)).cuda()
+    recv_x = torch.randn(rows, w.d, device="cuda").to(td)
+    x_local = torch.empty_like(recv_x)
+    y_recv = torch.empty_like(recv_x)
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    src = torch.empty(rows, dtype=torch.int32, device="cuda")
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    t_re, t_un = [], []
+    for i in range(steps + 3):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        ev[0].record(stream)
+        B.ep_regroup(G, E, rc, recv_x, x_local, off, src, w.dtype)
+        ev[1].record(stream)
+        flush.zero_()
+        ev[2].record(stream)
+        B.ep_ungroup(src, x_local, y_recv, w.dtype)
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            t_re.append(ev[0].elapsed_time(ev[1]))
+            t_un.append(ev[2].elapsed_time(ev[3]))
+    st = B.get_error()
+    if st != B.MOE_OK:
+        raise RuntimeError(f"device error in the expert-parallel kernels: {B.status_string(st)}")
+    ok = bool(torch.equal(y_recv, recv_x))          # ungroup inverts regroup
+    byt = 2 * rows * w.d * es
+    re_ms, un_ms = float(np.median(t_re)), float(np.median(t_un))
+    return {"ranks": G, "local_experts": E, "rows": rows, "algorithmic_bytes_per_kernel": byt,
+            "regroup_us": re_ms * 1e3, "ungroup_us": un_ms * 1e3,
+            "regroup_gbs": byt / (re_ms * 1e-3) / 1e9, "ungroup_gbs": byt / (un_ms * 1e-3) / 1e9,
+            "regroup_frac_hbm": byt / (re_ms * 1e-3) / 1e9 / hbm_gbs,
+            "ungroup_frac_hbm": byt / (un_ms * 1e-3) / 1e9 / hbm_gbs,
+            "peak_gbs": hbm_gbs, "ungroup_inverts_regroup": ok,
+            "timing": f"median of {steps} launches each, CUDA events, L2 flushed before each launch"}
 
 
 def main():
@@ -680,6 +739,10 @@ def main():
             fma = fma_peak_tflops(torch, torch.cuda.get_device_properties(local).multi_processor_count)
         except (OSError, RuntimeError):
             fma = None
+    # the expert-parallel receiving rank's local kernels at the headline workload's size (8 ranks)
+    ep_local = None
+    if rank == 0 and w.N % 8 == 0 and args.routing == "token" and args.capacity_factor is None:
+        ep_local = measure_ep_local(w, r["cnt"], torch, B, 8, r["P"]["hbm"])
     # the decode-shaped layer (HBM-bound on its active experts' weights), timed after the headline run
     dec = None
     decode_name = "decode-t32-n64-k8"
@@ -700,7 +763,8 @@ def main():
                    "forward_frac_hbm": rd["roof"]["forward_frac_hbm"],
                    "forward_algorithmic_bytes": rd["fwd_bytes"], "peak_gbs": rd["P"]["hbm"],
                    "active_experts": int((rd["cnt"] > 0).sum()), "route_roofline": route_roofline(rd, fma),
-                   "clocks": rd["clocks"], "cpu_baseline": rd["cpu"], "e2e": rd["e2e"],
+                   "clocks": rd["clocks"], "clocks_staged": rd["clocks_staged"], "cpu_baseline": rd["cpu"],
+                   "e2e": rd["e2e"],
                    "steps": max(args.steps, 50), "warmup": max(args.warmup, 10)}
     if rank != 0:
         if dist:
@@ -718,9 +782,10 @@ def main():
                    "routing": "expert choice, C = T*k/N = %d tokens per expert" % C if ec else "token choice (top-k)", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (2 x 126 MB write, then 2 x 126 MB read of another buffer); expert weights also exceed L2"},
         "timing": ("median over the timed steps, each one CUDA-graph replay of the whole step between two CUDA "
-                   "events on the stream; stage_ms: median over as many later steps (after a 0.5 s pause) in "
-                   "which each stage is its own graph replay between event pairs (their sum, "
-                   "staged_sum_of_stages, adds the gaps between replays)"
+                   "events on the stream; stage_ms: median over as many later steps (after a 0.5 s pause), each "
+                   "run alone (synchronised, 20 ms apart), in which each stage is its own graph replay between "
+                   "event pairs (their sum, staged_sum_of_stages, adds the gaps between replays); the roofline "
+                   "fractions use these stage times, clocks_staged their clock record"
                    if r["graphs"] else "median over steps of eager stage calls between CUDA events"),
         "ffn_tflops": r["ffn_flops"] / (r["ffn_ms"] * 1e-3) / 1e12,
         "layer_tflops": acc.layer_flops(w.T, w.d, w.N, w.k, w.F, w.act) / (r["step_ms"] * 1e-3) / 1e12,
@@ -735,6 +800,8 @@ def main():
         "gpu_launches": args.steps * (6 if ec else (1 + (1 if w.T * w.k <= 2048 else (3 if r["gather"] else 4))
                                                         + 2 + 1)),
         "clocks": r["clocks"],
+        "clocks_staged": r["clocks_staged"],
+        "ep_local": ep_local,
         "decode": dec,
         "kernel_source": kernel_source_hash(),
     }

@@ -53,10 +53,12 @@ struct RouteCfg {
   static constexpr int NP = EG * EPT;
   static constexpr int TG = THR / EG;
   static constexpr int TM = TG * TPT;
-  static constexpr int STAGES = NP >= 128 ? 3 : 4;
   static constexpr int XROW = kRouteBK * static_cast<int>(sizeof(TX)) + 16;  // bytes per token row (+pad)
   static constexpr int XBYTES = TM * XROW;                                   // one stage of x
   static constexpr int WBYTES = kRouteBK * NP * 4;                           // one stage of W_g
+  // few experts: a slice is computed quickly, so more slices stay in flight (about 48 KB)
+  static constexpr int SFEW = 49152 / (XBYTES + WBYTES);
+  static constexpr int STAGES = NP >= 128 ? 3 : (NP >= 32 ? 4 : (SFEW < 4 ? 4 : (SFEW > 12 ? 12 : SFEW)));
   static constexpr size_t kPipe = static_cast<size_t>(STAGES) * (XBYTES + WBYTES);
   static constexpr size_t kLogits = sizeof(float) * TM * (NP + 1);
   // per-warp statistics rows [THR / 32][2*NP + 1] after the logit tile
@@ -353,6 +355,28 @@ __global__ void __launch_bounds__(THR) route_kernel(const TX* __restrict__ x, co
     const int st = kb % S;
     const uint8_t* xst = xs + st * C::XBYTES;
     const float* wst = ws + st * kRouteBK * NP;
+    if constexpr (EPT == 1 && TPT <= 2) {
+      // few chains per thread (few experts): the slice's shared loads first, then its FMAs, so their
+      // latency is paid once per slice instead of once per step
+      float xv[TPT][kRouteBK];
+      float wv[kRouteBK][EPT];
+#pragma unroll
+      for (int i = 0; i < TPT; ++i)
+#pragma unroll
+        for (int k8 = 0; k8 < kRouteBK; k8 += 8)
+          load_x8(reinterpret_cast<const TX*>(xst + (ty * TPT + i) * C::XROW) + k8, xv[i] + k8);
+#pragma unroll
+      for (int u = 0; u < kRouteBK; ++u)
+#pragma unroll
+        for (int m = 0; m < EPT; ++m) wv[u][m] = wst[u * NP + V * tx + V * EG * (m / V) + (m % V)];
+#pragma unroll
+      for (int u = 0; u < kRouteBK; ++u)
+#pragma unroll
+        for (int i = 0; i < TPT; ++i)
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xv[i][u], wv[u][j], acc[i][j]);
+      continue;
+    }
 #pragma unroll
     for (int k8 = 0; k8 < kRouteBK; k8 += 8) {
       float xv[TPT][8];

@@ -341,8 +341,11 @@ size_t moe_forward_hostio_pipelined_workspace_size(const moe_shape *s);
  * cudaMalloc, cudaFree or allocating library routine.
  *
  * The first call on a device looks up that device's address of the array
- * (cudaGetSymbolAddress, with the device current); make that first call
- * before any stream capture. All calls share the one array and it keeps the
+ * (cudaGetSymbolAddress, with the device current; under a mutex, so first
+ * calls from several host threads are safe); make that first call before any
+ * stream capture. The cached address is not valid across a device reset
+ * (cudaDeviceReset): do not call this after one in the same process. All
+ * calls share the one array and it keeps the
  * last call's contents (every entry a call reads is written first by the same
  * call, so nothing needs clearing); calls whose work overlaps on the GPU (two
  * streams at once) race on it and must be serialised by the caller.

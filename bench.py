@@ -704,7 +704,7 @@ def main():
                     help="grouping without x_perm; the grouped GEMM gathers token rows through perm")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the decode-shaped sub-record that follows the headline workload")
-    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs"],
+    ap.add_argument("--ffn-tiling", default="auto", choices=["auto", "rows", "tokens", "pairs", "rowpairs"],
                     help="tensor-core tiling of the grouped GEMMs (library default: auto)")
     ap.add_argument("--capacity-factor", type=float, default=None,
                     help="expert capacity ceil(cf * T * k / N); overflow assignments are dropped")

@@ -407,13 +407,26 @@ moe_status moe_ep_ungroup(int64_t rows, int32_t d, int32_t dtype, const int32_t 
  *                      MMA (256 weight rows per MMA, each SM holding half of
  *                      the tile's tokens): four 48 KB pipeline stages per SM
  *                      instead of three 64 KB ones.
+ *   MOE_TILING_ROW_PAIRS row tiles computed by clusters of two SMs sharing each
+ *                      MMA: 256 permuted rows x 256 weight rows per tile, 128
+ *                      of each in each SM, so every weight tile serves twice the
+ *                      rows of MOE_TILING_ROWS. Used where the tile's output
+ *                      columns divide the GEMM's (SwiGLU F % 128, GELU F % 256,
+ *                      the down projection d % 256) and the rows are permuted
+ *                      (not moe_grouped_ffn_gather); row tiles otherwise.
  *   MOE_TILING_AUTO    per GEMM: token tiles on SM pairs when T*k >= 64*N and
  *                      the GEMM's reduction length (d for the first, F for the
  *                      second) is >= 4096, else row tiles (default).
  * The pages' grouped GEMM ("MoE显存与计算开销四阶段手算指南" section 4.3)
  * fixes no tiling; this only chooses how the same product is blocked.
  */
-typedef enum { MOE_TILING_AUTO = 0, MOE_TILING_ROWS = 1, MOE_TILING_TOKENS = 2, MOE_TILING_PAIRS = 3 } moe_tiling;
+typedef enum {
+    MOE_TILING_AUTO = 0,
+    MOE_TILING_ROWS = 1,
+    MOE_TILING_TOKENS = 2,
+    MOE_TILING_PAIRS = 3,
+    MOE_TILING_ROW_PAIRS = 4
+} moe_tiling;
 moe_status moe_set_ffn_tiling(int mode);
 int moe_get_ffn_tiling(void);
 

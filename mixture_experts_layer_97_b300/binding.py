@@ -24,7 +24,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_CORRUPT = 4, 5, 6
 MOE_F32, MOE_BF16 = 0, 1
 MOE_SWIGLU, MOE_GELU_TANH = 0, 1
-TILING = {"auto": 0, "rows": 1, "tokens": 2, "pairs": 3}
+TILING = {"auto": 0, "rows": 1, "tokens": 2, "pairs": 3, "rowpairs": 4}
 ACT = {"swiglu": MOE_SWIGLU, "gelu_tanh": MOE_GELU_TANH}
 DTYPE = {"f32": MOE_F32, "bf16": MOE_BF16}
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}

@@ -22,6 +22,7 @@
 #include "ffn_tc.cuh"
 #include "ffn_tc_swap.cuh"
 #include "ffn_tc_pair.cuh"
+#include "ffn_tc_rowpair.cuh"
 #include "permute.cuh"
 #include "route.cuh"
 
@@ -361,7 +362,8 @@ EncodeTiledFn encode_fn() {
 std::atomic<int> g_ffn_tiling{MOE_TILING_AUTO};
 
 bool tiling_valid(int mode) {
-  return mode == MOE_TILING_AUTO || mode == MOE_TILING_ROWS || mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS;
+  return mode == MOE_TILING_AUTO || mode == MOE_TILING_ROWS || mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS ||
+         mode == MOE_TILING_ROW_PAIRS;
 }
 
 // bf16 matrix [rows, cols] row-major; box = box_rows x box_cols columns with the
@@ -503,6 +505,48 @@ moe_status launch_tc_pair(const moe_shape* s, const RowSource& src, int K, const
   return launched();
 }
 
+// Row tiles on SM pairs: clusters of two CTAs sharing each MMA (256 permuted
+// rows x 256 weight rows per tile, 128 of each in each CTA).
+template <int EPI>
+moe_status launch_tc_rowpair(const moe_shape* s, const void* a, int K, const void* b0, const void* b1, int Nout,
+                             const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
+  constexpr int HB = rp_tile_cols<EPI>();
+  const int64_t A = n_assign(s);
+  CUtensorMap ma, mb0, mb1;
+  if (!make_map(&ma, a, static_cast<uint64_t>(A), static_cast<uint64_t>(K), kRpHalf)) return MOE_ERR_CUDA;
+  const uint64_t brows = static_cast<uint64_t>(s->N) * Nout;
+  if (!make_map(&mb0, b0, brows, static_cast<uint64_t>(K), kRpHalf)) return MOE_ERR_CUDA;
+  if (EPI == EPI_SWIGLU) {
+    if (!make_map(&mb1, b1, brows, static_cast<uint64_t>(K), kRpHalf)) return MOE_ERR_CUDA;
+  } else {
+    mb1 = mb0;
+  }
+  auto kern = grouped_gemm_tc_rowpair_kernel<EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRpSmemBytes)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int64_t n_tiles = Nout / HB;
+  const int64_t pairs_needed = ((A + kRpBM - 1) / kRpBM + s->N) * n_tiles;
+  const int64_t max_pairs = num_sms() / 2;
+  const int64_t pairs = pairs_needed < max_pairs ? pairs_needed : max_pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kRpThreads, 1, 1);
+  cfg.dynamicSmemBytes = kRpSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, ma, mb0, mb1, offsets, s->N, static_cast<int>(A), K, Nout,
+                         static_cast<__nv_bfloat16*>(out), ldo, kWaitTimeoutNs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launched();
+}
+
 template <int EPI>
 moe_status launch_tc_swap(const moe_shape* s, const RowSource& src, int K, const void* w0, const void* w1, int Nout,
                           const int32_t* offsets, void* out, int ldo, cudaStream_t st, int mode, int* tile_counter) {
@@ -518,7 +562,7 @@ moe_status launch_tc_swap(const moe_shape* s, const RowSource& src, int K, const
 // expert holds enough rows to fill tiles and K is long enough to hide it.
 bool use_token_tiles(const moe_shape* s, int K, int mode) {
   if (mode == MOE_TILING_TOKENS || mode == MOE_TILING_PAIRS) return true;
-  if (mode == MOE_TILING_ROWS) return false;
+  if (mode == MOE_TILING_ROWS || mode == MOE_TILING_ROW_PAIRS) return false;
   return n_assign(s) >= static_cast<int64_t>(kAutoTokenTileMinRowsPerExpert) * s->N && K >= kAutoTokenTileMinK;
 }
 
@@ -551,7 +595,14 @@ moe_status ffn_impl(const moe_shape* s, const RowSource& src, const int32_t* off
   int* ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ffn_h_bytes(s));
   moe_status r;
   if (s->dtype == MOE_BF16) {
-    if (use_token_tiles(s, d, mode))
+    // row tiles on SM pairs where the tile's columns divide the output (permuted rows only)
+    const bool rp1 = mode == MOE_TILING_ROW_PAIRS && src.perm == nullptr &&
+                     F % (s->act == MOE_SWIGLU ? rp_tile_cols<EPI_SWIGLU>() : rp_tile_cols<EPI_GELU>()) == 0;
+    const bool rp2 = mode == MOE_TILING_ROW_PAIRS && d % rp_tile_cols<EPI_PLAIN>() == 0;
+    if (rp1)
+      r = (s->act == MOE_SWIGLU) ? launch_tc_rowpair<EPI_SWIGLU>(s, src.a, d, w_gate, w_up, F, offsets, h, F, st)
+                                 : launch_tc_rowpair<EPI_GELU>(s, src.a, d, w_gate, nullptr, F, offsets, h, F, st);
+    else if (use_token_tiles(s, d, mode))
       r = (s->act == MOE_SWIGLU)
               ? launch_tc_swap<EPI_SWIGLU>(s, src, d, w_gate, w_up, F, offsets, h, F, st, mode, ctr)
               : launch_tc_swap<EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st, mode, ctr);
@@ -562,6 +613,7 @@ moe_status ffn_impl(const moe_shape* s, const RowSource& src, const int32_t* off
       r = (F % 256 == 0) ? launch_tc<256, EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st)
                          : launch_tc<128, EPI_GELU>(s, src, d, w_gate, nullptr, F, offsets, h, F, st);
     if (r != MOE_OK) return r;
+    if (rp2) return launch_tc_rowpair<EPI_PLAIN>(s, h, F, w_down, nullptr, d, offsets, y_perm, d, st);
     if (use_token_tiles(s, F, mode))
       return launch_tc_swap<EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st, mode, ctr);
     return (d % 256 == 0) ? launch_tc<256, EPI_PLAIN>(s, hs, F, w_down, nullptr, d, offsets, y_perm, d, st)

@@ -131,7 +131,7 @@ def test_binding_refuses_cpu_tensors(L):
 
 def test_tiling_policy_setter(L):
     assert B.get_ffn_tiling() == "auto"
-    for m in ("rows", "tokens", "pairs", "auto"):
+    for m in ("rows", "tokens", "pairs", "rowpairs", "auto"):
         B.set_ffn_tiling(m)
         assert B.get_ffn_tiling() == m
     assert L.moe_set_ffn_tiling(7) == B.MOE_ERR_INVALID_ARG

@@ -64,7 +64,7 @@ RAGGED = [0, 1, 127, 128, 129, 300, 0, 5]
 RAGGED_TOKENS = [16, 17, 256, 257, 0, 31, 513, 1500]
 
 
-@pytest.fixture(params=["rows", "tokens", "pairs"])
+@pytest.fixture(params=["rows", "tokens", "pairs", "rowpairs"])
 def tiling(request):
     B.set_ffn_tiling(request.param)
     yield request.param
@@ -170,7 +170,7 @@ def test_tilings_agree_within_tolerance():
     of each other."""
     w, xp, ws, off = make_case([200, 0, 300, 45, 1000], 512, 384, "swiglu", "bf16", 12)
     outs = {}
-    for mode in ("rows", "tokens", "pairs"):
+    for mode in ("rows", "tokens", "pairs", "rowpairs"):
         B.set_ffn_tiling(mode)
         outs[mode] = run_ffn(w, xp, ws, off)
     B.set_ffn_tiling("auto")
@@ -179,6 +179,7 @@ def test_tilings_agree_within_tolerance():
         assert rel_err(got, ref) <= tol("bf16"), mode
     assert rel_err(outs["rows"], outs["tokens"]) <= tol("bf16")
     assert rel_err(outs["pairs"], outs["tokens"]) <= tol("bf16")
+    assert rel_err(outs["rowpairs"], outs["rows"]) <= tol("bf16")
 
 
 @pytest.mark.parametrize("T,N,k,d,F,act", [(300, 8, 2, 256, 384, "swiglu"), (1000, 16, 4, 512, 256, "gelu_tanh"),

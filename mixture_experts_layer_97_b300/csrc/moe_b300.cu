@@ -566,6 +566,16 @@ bool use_token_tiles(const moe_shape* s, int K, int mode) {
   return n_assign(s) >= static_cast<int64_t>(kAutoTokenTileMinRowsPerExpert) * s->N && K >= kAutoTokenTileMinK;
 }
 
+// Row tiles on SM pairs (MOE_TILING_ROW_PAIRS only), where their output
+// columns divide the GEMM's and its rows are the permuted copy. Auto does not
+// take them: on the skewed batch they are within 1-2 % of row tiles (581 + 374
+// against 589 + 379 us per launch), with a capacity of 1.25 on the same batch
+// 6 % slower (most experts then hold few rows, and a 256-row tile of them is
+// mostly padding), on decode 8 % slower.
+bool use_row_pairs(int mode, int cols, int tile_cols, bool permuted) {
+  return mode == MOE_TILING_ROW_PAIRS && permuted && cols % tile_cols == 0;
+}
+
 template <int EPI>
 moe_status launch_simt(const moe_shape* s, const void* a, int K, const void* b0, const void* b1, int Nout,
                        const int32_t* offsets, void* out, int ldo, cudaStream_t st) {
@@ -595,10 +605,9 @@ moe_status ffn_impl(const moe_shape* s, const RowSource& src, const int32_t* off
   int* ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + ffn_h_bytes(s));
   moe_status r;
   if (s->dtype == MOE_BF16) {
-    // row tiles on SM pairs where the tile's columns divide the output (permuted rows only)
-    const bool rp1 = mode == MOE_TILING_ROW_PAIRS && src.perm == nullptr &&
-                     F % (s->act == MOE_SWIGLU ? rp_tile_cols<EPI_SWIGLU>() : rp_tile_cols<EPI_GELU>()) == 0;
-    const bool rp2 = mode == MOE_TILING_ROW_PAIRS && d % rp_tile_cols<EPI_PLAIN>() == 0;
+    const bool rp1 = use_row_pairs(mode, F, s->act == MOE_SWIGLU ? rp_tile_cols<EPI_SWIGLU>() : rp_tile_cols<EPI_GELU>(),
+                                   src.perm == nullptr);
+    const bool rp2 = use_row_pairs(mode, d, rp_tile_cols<EPI_PLAIN>(), true);
     if (rp1)
       r = (s->act == MOE_SWIGLU) ? launch_tc_rowpair<EPI_SWIGLU>(s, src.a, d, w_gate, w_up, F, offsets, h, F, st)
                                  : launch_tc_rowpair<EPI_GELU>(s, src.a, d, w_gate, nullptr, F, offsets, h, F, st);

@@ -6,7 +6,9 @@ all experts' contiguous rows with expert offsets) blocks each expert's rows in
 one of two ways, and the full-size tests must compare at least one row of
 every block the kernels produce:
 
-  row tiles     an expert's c rows in 128-row tiles [128 i, min(c, 128 (i+1)))
+  row tiles     an expert's c rows in 128-row tiles [128 i, min(c, 128 (i+1)));
+                on SM pairs a 256-row tile's two CTAs hold its 128-row halves,
+                which are exactly these 128-row blocks
   token tiles   ntt = ceil(c / 256) tiles of base = roundup16(ceil(c / ntt))
                 rows, tile i = [i base, min(c, (i+1) base)); the MMA's N side
                 is the tile's rows rounded up to 16 (nt). On SM pairs each CTA

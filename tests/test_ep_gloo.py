@@ -38,7 +38,7 @@ def _rank_main(rank, world, port, out):
     try:
         w = rank_workload(rank)
         # tokens of this rank: rows of a larger seeded batch, disjoint per rank
-        big = w.scaled(T=400)
+        big = w.scaled(T=1000)
         lo = sum(rank_workload(r).T for r in range(rank))
         x = S.x_rows(big, lo, lo + w.T)
         part = ep.Partition(w.N, world)
@@ -53,7 +53,7 @@ def _rank_main(rank, world, port, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("world", [1, 2, 4, 8])
 def test_expert_parallel_forward_equals_single_process_oracle(world):
     port = _free_port()
     with mp.Manager() as m:

@@ -1,7 +1,7 @@
 """Expert parallelism on the host: the orchestration of
 mixture_experts_layer_97_b300.ep (count exchange, row all-to-all, regroup,
-local experts, ungroup, reverse all-to-all, combine) run by 2 and 4 gloo
-ranks, each step computed by the CPU oracle. Every rank's output must equal,
+local experts, ungroup, reverse all-to-all, combine) run by 1, 2, 4 and 8
+gloo ranks, each step computed by the CPU oracle. Every rank's output must equal,
 bit for bit in fp64, the single-process oracle forward of that rank's tokens
 with all N experts ("MoE混合专家模型计算原理与推理部署实战解析" section 3.3:
 splitting the experts over cards changes where a row is computed, not what)."""

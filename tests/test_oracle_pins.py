@@ -337,6 +337,26 @@ def test_forward_bruteforce_per_token_loop():
             assert f["perm"][f["inv_perm"][t * k + j]] == t
 
 
+def test_forward_is_equivariant_under_token_order():
+    """Tokens are independent ("MoE混合专家模型计算原理与推理部署实战解析"
+    section 2.2: each token is routed and mixed on its own): reordering the
+    batch reorders the output rows the same way and changes no value, while
+    the grouping (offsets, counts) only depends on the multiset of choices.
+    Catches a combine or permutation that mixes up token and slot indices."""
+    rng = np.random.default_rng(121)
+    T, d, N, k, F = 23, 16, 6, 3, 20
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    wg = (rng.standard_normal((d, N)) * 0.5).astype(np.float32)
+    WG = rng.standard_normal((N, F, d)) * 0.2
+    WU = rng.standard_normal((N, F, d)) * 0.2
+    WD = rng.standard_normal((N, d, F)) * 0.2
+    order = rng.permutation(T)
+    a = oracle.forward(x, wg, None, WG, WU, WD, k, "swiglu")
+    b = oracle.forward(x[order], wg, None, WG, WU, WD, k, "swiglu")
+    np.testing.assert_array_equal(b["out"], a["out"][order])
+    np.testing.assert_array_equal(b["counts"], a["counts"])
+
+
 def test_combine_one_hot_and_order():
     y = np.arange(12, dtype=np.float64).reshape(4, 3)
     inv = np.array([2, 0, 3, 1], np.int32)     # T=2, k=2

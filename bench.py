@@ -742,7 +742,10 @@ def main():
     # the expert-parallel receiving rank's local kernels at the headline workload's size (8 ranks)
     ep_local = None
     if rank == 0 and w.N % 8 == 0 and args.routing == "token" and args.capacity_factor is None:
-        ep_local = measure_ep_local(w, r["cnt"], torch, B, 8, r["P"]["hbm"])
+        try:
+            ep_local = measure_ep_local(w, r["cnt"], torch, B, 8, r["P"]["hbm"])
+        except (RuntimeError, torch.cuda.OutOfMemoryError) as exc:   # a side record: never costs the line
+            ep_local = {"error": str(exc).splitlines()[0]}
     # the decode-shaped layer (HBM-bound on its active experts' weights), timed after the headline run
     dec = None
     decode_name = "decode-t32-n64-k8"
